@@ -1,0 +1,57 @@
+"""Plant plausible mistakes in a COPY of the oracle source (on the CPU) and check that
+the pins in test_oracle_pins.py catch every one of them.
+
+Each mutant is the oracle's C source with one textual change: a dropped term, a wrong
+sign, a wrong index, a transposed operand, an off-by-one in a mask.  A mutant that no
+pin rejects would mean the pins leave that part of the oracle unchecked.
+"""
+import os
+import tempfile
+
+import pytest
+
+from oracle import oracle as orc
+import test_oracle_pins as pins
+
+MUTANTS = {
+    "tail_mask_off_by_one": ("(j % block) >= valid", "(j % block) > valid"),
+    "lse_natural_log": ("lse[t * block + r] = (m + log(l)) / log(2.0);",
+                        "lse[t * block + r] = m + log(l);"),
+    "score_reads_query_row_of_k": ("bf16_to_double(kh[(int64_t)j * D + d])",
+                                   "bf16_to_double(kh[(int64_t)i * D + d])"),
+    "no_normalisation": ("orow[d] = acc[d] / l;", "orow[d] = acc[d];"),
+    "exp_sign": ("const double p = exp(s_buf[a] - m);", "const double p = exp(m - s_buf[a]);"),
+    "scale_dropped": ("s_buf[n_att] = scale * dot;", "s_buf[n_att] = dot;"),
+    "count_not_clamped_reads_padding": ("for (int s = 0; s < n; ++s) {",
+                                        "for (int s = 0; s < max_kv; ++s) {"),
+    "range_check_dropped": ("if (kb >= 0 && kb < nb) mrow[kb] = 1;",
+                            "if (kb >= 0 && kb < nb) mrow[kb] = 1; else if (kb >= 0) mrow[kb % nb] = 1;"),
+    "mask_strides_swapped": ("(b * mask_stride_b + h * mask_stride_h)",
+                             "(b * mask_stride_h + h * mask_stride_b)"),
+    "v_row_from_query": ("vh + (int64_t)j_buf[a] * D", "vh + (int64_t)i * D"),
+    "empty_row_lse_zero": ("lse[t * block + r] = ORACLE_LSE_EMPTY;", "lse[t * block + r] = 0.0;"),
+    "lut_padding_zero": ("for (int s = n; s < max_kv; ++s) irow[s] = -1;",
+                         "for (int s = n; s < max_kv; ++s) irow[s] = 0;"),
+    "lut_descending": ("for (int kb = 0; kb < nb; ++kb) {\n      if (mrow[kb] != 0) {",
+                       "for (int kb = nb - 1; kb >= 0; --kb) {\n      if (mrow[kb] != 0) {"),
+    "bitmap_byte_must_be_one": ("if (mrow[kb] != 0) {", "if (mrow[kb] == 1) {"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name):
+    src = open(orc.SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, "mutation anchor must be unique: " + name
+    with tempfile.TemporaryDirectory() as d:
+        msrc = os.path.join(d, "mutant.c")
+        open(msrc, "w").write(src.replace(old, new))
+        lib = orc.build(msrc, os.path.join(d, "libmutant.so"), openmp=False)
+        h = orc.load(lib, msrc)
+        caught = []
+        for pin in pins.PINS:
+            try:
+                pin(h)
+            except AssertionError:
+                caught.append(pin.__name__)
+        assert caught, "no pin rejects mutant " + name
