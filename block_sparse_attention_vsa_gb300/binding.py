@@ -1,0 +1,243 @@
+"""Thin Python binding over libvsa_gb300.so (include/vsa.h): argument marshalling only.
+
+Every step of the forward pass and of the metadata conversions runs in the library's
+CUDA kernels.  Torch is used for device memory, streams and dtype checks; there is no
+CPU or eager-PyTorch fallback -- if the library is missing or was built for another
+GPU the calls raise.
+
+Functions mirror the C entry points:
+  vsa_fwd, jenga_fwd, vsa_lut_to_bitmap, vsa_bitmap_to_lut, vsa_fwd_from_host,
+  vsa_device_status, vsa_workspace_bytes
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libvsa_gb300.so")
+
+VSA_OK, VSA_ERR_INVALID_ARG, VSA_ERR_UNSUPPORTED, VSA_ERR_CUDA, VSA_ERR_DEVICE_TIMEOUT = range(5)
+LSE_EMPTY = -3.4028234663852886e38  # -FLT_MAX, the lse of a row with no attended key
+HEAD_DIM = 128
+MAX_BLOCKS = 2048
+
+# every symbol include/vsa.h declares
+EXPORTS = ("vsa_fwd", "jenga_fwd", "vsa_workspace_bytes", "vsa_lut_to_bitmap",
+           "vsa_bitmap_to_lut", "vsa_fwd_from_host", "vsa_device_status",
+           "vsa_last_launch_count", "vsa_status_str")
+
+
+class VsaError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} (status {code})")
+        self.code = code
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the library and declare its signatures (no CUDA call happens here)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -m block_sparse_attention_vsa_gb300.build`"
+            " (nvcc, sm_103a); there is no fallback implementation")
+    h = ctypes.CDLL(path)
+    P, i32, f32, sz, u = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t,
+                          ctypes.c_uint)
+    h.vsa_fwd.restype = i32
+    h.vsa_fwd.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P, P, P]
+    h.jenga_fwd.restype = i32
+    h.jenga_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P, P, P]
+    h.vsa_workspace_bytes.restype = sz
+    h.vsa_workspace_bytes.argtypes = []
+    h.vsa_lut_to_bitmap.restype = i32
+    h.vsa_lut_to_bitmap.argtypes = [P, P, i32, i32, i32, P, P]
+    h.vsa_bitmap_to_lut.restype = i32
+    h.vsa_bitmap_to_lut.argtypes = [P, i32, i32, i32, P, P, P]
+    h.vsa_fwd_from_host.restype = i32
+    h.vsa_fwd_from_host.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P,
+                                    P, P, P, P, P, P, P, P, P, P]
+    h.vsa_device_status.restype = i32
+    h.vsa_device_status.argtypes = [P, ctypes.POINTER(u)]
+    h.vsa_last_launch_count.restype = i32
+    h.vsa_last_launch_count.argtypes = []
+    h.vsa_status_str.restype = ctypes.c_char_p
+    h.vsa_status_str.argtypes = [i32]
+    _lib = h
+    return h
+
+
+def _check(fn: str, code: int):
+    if code != VSA_OK:
+        raise VsaError(fn, code, load().vsa_status_str(code).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t, name, dtype, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must be {ndim}-D, got {t.dim()}-D")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _meta32(t, name):
+    """int64 metadata costs a cast (as the original wrapper does); int32 passes through."""
+    if t.dtype == torch.int64:
+        t = t.to(torch.int32)
+    return _dev(t.contiguous(), name, torch.int32)
+
+
+def workspace_bytes() -> int:
+    return int(load().vsa_workspace_bytes())
+
+
+def new_workspace(device=None) -> torch.Tensor:
+    """A zeroed scheduling workspace; each forward call leaves it zero again."""
+    n = (workspace_bytes() + 3) // 4
+    return torch.zeros(n, dtype=torch.int32, device=device or "cuda")
+
+
+def vsa_fwd(q, k, v, q2k_idx, q2k_num, variable_block_sizes, block=None, scale=None, out=None,
+            lse=True, workspace=None, stream=None):
+    """VSA forward.  q, k, v: bf16 [B,H,S,128]; q2k_idx [B,H,nb,max_kv]; q2k_num [B,H,nb];
+    variable_block_sizes [nb].  Returns (out, lse or None).  ``lse`` may be True (allocate),
+    False/None (skip, the inference route) or a float32 [B,H,S] tensor to write into."""
+    h = load()
+    _dev(q, "q", torch.bfloat16, 4)
+    _dev(k, "k", torch.bfloat16, 4)
+    _dev(v, "v", torch.bfloat16, 4)
+    B, H, S, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape")
+    vbs = _meta32(variable_block_sizes, "variable_block_sizes")
+    nb = vbs.numel()
+    if block is None:
+        block = S // nb if nb and S % nb == 0 else 0
+    idx = _meta32(q2k_idx, "q2k_idx")
+    num = _meta32(q2k_num, "q2k_num")
+    if idx.dim() != 4 or idx.shape[:3] != (B, H, nb) or num.shape != (B, H, nb):
+        raise ValueError("q2k_idx must be [B,H,nb,max_kv] and q2k_num [B,H,nb]")
+    max_kv = idx.shape[-1]
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _dev(out, "out", torch.bfloat16, 4)
+    if lse is True:
+        lse_t = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    elif lse is None or lse is False:
+        lse_t = None
+    else:
+        lse_t = _dev(lse, "lse", torch.float32, 3)
+    code = h.vsa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(num), _ptr(vbs), B, H, S, D,
+                     max_kv, block, scale, _ptr(out), _ptr(lse_t), _ptr(workspace),
+                     _stream(stream))
+    _check("vsa_fwd", code)
+    return out, lse_t
+
+
+def jenga_fwd(q, k, v, mask_bitmap, block_q=64, block_k=64, scale=None, out=None, lse=True,
+              workspace=None, stream=None):
+    """Jenga forward from an i8 bitmap [S/block_q, S/block_k] shared by every (b, h)."""
+    h = load()
+    _dev(q, "q", torch.bfloat16, 4)
+    _dev(k, "k", torch.bfloat16, 4)
+    _dev(v, "v", torch.bfloat16, 4)
+    B, H, S, D = q.shape
+    if mask_bitmap.dtype == torch.bool:
+        mask_bitmap = mask_bitmap.to(torch.int8)
+    _dev(mask_bitmap, "mask_bitmap", torch.int8, 2)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is True:
+        lse_t = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    elif lse is None or lse is False:
+        lse_t = None
+    else:
+        lse_t = _dev(lse, "lse", torch.float32, 3)
+    code = h.jenga_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(mask_bitmap), B, H, S, D, block_q,
+                       block_k, scale, _ptr(out), _ptr(lse_t), _ptr(workspace), _stream(stream))
+    _check("jenga_fwd", code)
+    return out, lse_t
+
+
+def vsa_lut_to_bitmap(q2k_idx, q2k_num, nb, stream=None):
+    """[..., rows, max_kv] + [..., rows] -> int8 [..., rows, nb] (bit-exact 0/1)."""
+    h = load()
+    idx = _meta32(q2k_idx, "q2k_idx")
+    num = _meta32(q2k_num, "q2k_num")
+    max_kv = idx.shape[-1]
+    rows = num.numel()
+    out = torch.empty(tuple(num.shape) + (nb,), dtype=torch.int8, device=idx.device)
+    _check("vsa_lut_to_bitmap",
+           h.vsa_lut_to_bitmap(_ptr(idx), _ptr(num), rows, max_kv, nb, _ptr(out), _stream(stream)))
+    return out
+
+
+def vsa_bitmap_to_lut(bitmap, max_kv, stream=None):
+    """int8 [..., rows, nb] -> (int32 [..., rows, max_kv] ascending, -1 padded; int32 [..., rows])."""
+    h = load()
+    if bitmap.dtype == torch.bool:
+        bitmap = bitmap.to(torch.int8)
+    _dev(bitmap, "bitmap", torch.int8)
+    nb = bitmap.shape[-1]
+    rows = bitmap.numel() // nb
+    idx = torch.empty(tuple(bitmap.shape[:-1]) + (max_kv,), dtype=torch.int32, device=bitmap.device)
+    num = torch.empty(tuple(bitmap.shape[:-1]), dtype=torch.int32, device=bitmap.device)
+    _check("vsa_bitmap_to_lut",
+           h.vsa_bitmap_to_lut(_ptr(bitmap), rows, nb, max_kv, _ptr(idx), _ptr(num),
+                               _stream(stream)))
+    return idx, num
+
+
+def vsa_fwd_from_host(h_q, h_k, h_v, h_idx, h_num, h_vbs, block, scale, h_out, h_lse, dev_bufs,
+                      workspace=None, stream=None):
+    """Host-buffer entry: copies in, runs vsa_fwd, copies out -- all enqueued on ``stream``.
+    ``dev_bufs`` = dict of device tensors q, k, v, idx, num, vbs, out, lse (lse may be None)."""
+    h = load()
+    B, H, S, D = h_q.shape
+    max_kv = h_idx.shape[-1]
+    d = dev_bufs
+    code = h.vsa_fwd_from_host(_ptr(h_q), _ptr(h_k), _ptr(h_v), _ptr(h_idx), _ptr(h_num),
+                               _ptr(h_vbs), B, H, S, D, max_kv, block, float(scale), _ptr(h_out),
+                               _ptr(h_lse), _ptr(d["q"]), _ptr(d["k"]), _ptr(d["v"]),
+                               _ptr(d["idx"]), _ptr(d["num"]), _ptr(d["vbs"]), _ptr(d["out"]),
+                               _ptr(d.get("lse")), _ptr(workspace), _stream(stream))
+    _check("vsa_fwd_from_host", code)
+
+
+def vsa_device_status(stream=None):
+    """(status code, detail) of the device status word; synchronises the stream."""
+    h = load()
+    detail = ctypes.c_uint(0)
+    code = h.vsa_device_status(_stream(stream), ctypes.byref(detail))
+    return code, detail.value
+
+
+def vsa_last_launch_count() -> int:
+    return int(load().vsa_last_launch_count())

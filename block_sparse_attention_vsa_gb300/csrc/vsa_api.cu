@@ -1,0 +1,361 @@
+// vsa_api.cu -- the C ABI of libvsa_gb300.so (declared in include/vsa.h): host-side
+// argument checks, TMA tensor-map encoding, persistent-grid launch of the forward
+// kernel, the metadata conversion kernels, the host-buffer wrapper and the device
+// status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/vsa.h"
+#include "vsa_fwd_kernel.cuh"
+
+namespace vsa {
+
+// Device status word: a kernel that gives up on a bounded wait records a code here.
+__device__ unsigned int g_status = 0;
+
+// ------------------------------------------------------------------ metadata kernels
+// LUT -> bitmap.  One CTA per row: zero the row, then scatter 1 at every listed block.
+__global__ void lut_to_bitmap_kernel(const int32_t* __restrict__ idx,
+                                     const int32_t* __restrict__ num, int max_kv, int nb,
+                                     int8_t* __restrict__ bitmap) {
+  const long long r = blockIdx.x;
+  int8_t* row = bitmap + r * nb;
+  for (int kb = threadIdx.x; kb < nb; kb += blockDim.x) row[kb] = 0;
+  __syncthreads();
+  int n = num[r];
+  n = n < 0 ? 0 : (n > max_kv ? max_kv : n);
+  const int32_t* lut = idx + r * max_kv;
+  for (int s = threadIdx.x; s < n; s += blockDim.x) {
+    const int kb = lut[s];
+    if (kb >= 0 && kb < nb) row[kb] = 1;
+  }
+}
+
+// bitmap -> LUT.  One warp per row: ascending ballot/popc compaction, then -1 padding.
+__global__ void bitmap_to_lut_kernel(const int8_t* __restrict__ bitmap, int rows, int nb,
+                                     int max_kv, int32_t* __restrict__ idx,
+                                     int32_t* __restrict__ num) {
+  const long long r = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x / 32);
+  if (r >= rows) return;
+  const unsigned lane = threadIdx.x & 31;
+  const int8_t* row = bitmap + r * nb;
+  int32_t* out = idx + r * max_kv;
+  int count = 0;
+  for (int base = 0; base < nb && count < max_kv; base += 32) {
+    const int kb = base + (int)lane;
+    const bool sel = kb < nb && row[kb] != 0;
+    const unsigned ballot = __ballot_sync(0xffffffffu, sel);
+    const int pos = count + __popc(ballot & ((1u << lane) - 1u));
+    if (sel && pos < max_kv) out[pos] = kb;
+    count += __popc(ballot);
+  }
+  if (count > max_kv) count = max_kv;
+  for (int s = count + (int)lane; s < max_kv; s += 32) out[s] = -1;
+  if (lane == 0) num[r] = count;
+}
+
+}  // namespace vsa
+
+using namespace vsa;
+
+namespace {
+
+thread_local int t_last_launches = 0;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sm_count = 0;
+  int major = 0, minor = 0;
+  bool attr_set[4] = {false, false, false, false};
+};
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+vsa_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return VSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return VSA_ERR_CUDA;
+    d.ready = true;
+  }
+  *out = &d;
+  return VSA_OK;
+}
+
+// 2-D view [rows, 128] of a BHSD bf16 tensor, 128-byte swizzle, box {64, box_rows}.
+bool make_map(CUtensorMap* m, const void* ptr, long long rows, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {128 * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb_) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb_ && y < x + na;
+}
+
+template <int BLOCK, bool JENGA>
+vsa_status launch_fwd(DeviceInfo* dev, int slot, const void* q, const void* k, const void* v,
+                      void* out, long long rows, const FwdArgs& args, cudaStream_t stream) {
+  auto kern = bsa_fwd_kernel<BLOCK, JENGA>;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!dev->attr_set[slot]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kSmemBytes) != cudaSuccess)
+        return VSA_ERR_CUDA;
+      dev->attr_set[slot] = true;
+    }
+  }
+  CUtensorMap tq, tk, tv, to;
+  if (!make_map(&tq, q, rows, 128) || !make_map(&tk, k, rows, BLOCK) ||
+      !make_map(&tv, v, rows, BLOCK) || !make_map(&to, out, rows, 128))
+    return VSA_ERR_CUDA;
+  const int grid = args.n_items < dev->sm_count ? args.n_items : dev->sm_count;
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, args);
+  if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
+  t_last_launches = 1;
+  return VSA_OK;
+}
+
+vsa_status common_checks(const void* q, const void* k, const void* v, const void* out, int B,
+                         int H, int S, int D, int block, float scale, DeviceInfo** dev,
+                         bool* nothing) {
+  *nothing = false;
+  if (B < 0 || H < 0 || S < 0) return VSA_ERR_INVALID_ARG;
+  if (D != VSA_HEAD_DIM) return VSA_ERR_UNSUPPORTED;
+  if (block != 64 && block != 128) return VSA_ERR_UNSUPPORTED;
+  if (!(scale > 0.0f) || !std::isfinite(scale)) return VSA_ERR_INVALID_ARG;
+  if (S % block != 0) return VSA_ERR_INVALID_ARG;
+  const int nb = S / block;
+  if (nb % 2 != 0) return VSA_ERR_UNSUPPORTED;
+  if (nb > VSA_MAX_BLOCKS) return VSA_ERR_UNSUPPORTED;
+  const long long rows = (long long)B * H * S;
+  if (rows > (long long)INT_MAX) return VSA_ERR_UNSUPPORTED;
+  if (rows == 0) {
+    *nothing = true;
+    return VSA_OK;
+  }
+  if (!q || !k || !v || !out) return VSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return VSA_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)rows * D * 2;
+  if (overlaps(out, bytes, q, bytes) || overlaps(out, bytes, k, bytes) ||
+      overlaps(out, bytes, v, bytes))
+    return VSA_ERR_INVALID_ARG;
+  vsa_status st = device_info(dev);
+  if (st != VSA_OK) return st;
+  if ((*dev)->major != 10 || (*dev)->minor != 3) return VSA_ERR_UNSUPPORTED;
+  return VSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t vsa_workspace_bytes(void) { return 256; }
+
+vsa_status vsa_fwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
+                   const int32_t* q2k_idx, const int32_t* q2k_num,
+                   const int32_t* variable_block_sizes, int B, int H, int S, int D, int max_kv,
+                   int block, float scale, vsa_bf16* out, float* lse, void* workspace,
+                   vsa_stream_t stream) {
+  t_last_launches = 0;
+  DeviceInfo* dev = nullptr;
+  bool nothing = false;
+  vsa_status st = common_checks(q, k, v, out, B, H, S, D, block, scale, &dev, &nothing);
+  if (st != VSA_OK || nothing) return st;
+  if (max_kv < 1) return VSA_ERR_INVALID_ARG;
+  if (!q2k_idx || !q2k_num || !variable_block_sizes) return VSA_ERR_INVALID_ARG;
+  if (lse && overlaps(lse, (size_t)B * H * S * 4, out, (size_t)B * H * S * D * 2))
+    return VSA_ERR_INVALID_ARG;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 3u)) return VSA_ERR_INVALID_ARG;
+  const int nb = S / block;
+  FwdArgs a{};
+  a.q2k_idx = q2k_idx;
+  a.q2k_num = q2k_num;
+  a.vbs = variable_block_sizes;
+  a.bitmap = nullptr;
+  a.lse = lse;
+  a.sched = static_cast<unsigned int*>(workspace);
+  unsigned int* status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_status) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  a.status = status;
+  a.H = H;
+  a.S = S;
+  a.nb = nb;
+  a.max_kv = max_kv;
+  a.n_items = (int)((long long)B * H * nb / (block == 64 ? 2 : 1));
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const long long rows = (long long)B * H * S;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (block == 64) return launch_fwd<64, false>(dev, 0, q, k, v, out, rows, a, s);
+  return launch_fwd<128, false>(dev, 1, q, k, v, out, rows, a, s);
+}
+
+vsa_status jenga_fwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
+                     const int8_t* mask_bitmap, int B, int H, int S, int D, int block_q,
+                     int block_k, float scale, vsa_bf16* out, float* lse, void* workspace,
+                     vsa_stream_t stream) {
+  t_last_launches = 0;
+  if (block_q != block_k) return VSA_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  bool nothing = false;
+  vsa_status st = common_checks(q, k, v, out, B, H, S, D, block_k, scale, &dev, &nothing);
+  if (st != VSA_OK || nothing) return st;
+  if (!mask_bitmap) return VSA_ERR_INVALID_ARG;
+  if (lse && overlaps(lse, (size_t)B * H * S * 4, out, (size_t)B * H * S * D * 2))
+    return VSA_ERR_INVALID_ARG;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 3u)) return VSA_ERR_INVALID_ARG;
+  const int block = block_k;
+  const int nb = S / block;
+  FwdArgs a{};
+  a.bitmap = mask_bitmap;
+  a.lse = lse;
+  a.sched = static_cast<unsigned int*>(workspace);
+  unsigned int* status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_status) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  a.status = status;
+  a.H = H;
+  a.S = S;
+  a.nb = nb;
+  a.max_kv = 1;
+  a.n_items = (int)((long long)B * H * nb / (block == 64 ? 2 : 1));
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const long long rows = (long long)B * H * S;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (block == 64) return launch_fwd<64, true>(dev, 2, q, k, v, out, rows, a, s);
+  return launch_fwd<128, true>(dev, 3, q, k, v, out, rows, a, s);
+}
+
+vsa_status vsa_lut_to_bitmap(const int32_t* q2k_idx, const int32_t* q2k_num, int rows,
+                             int max_kv, int nb, int8_t* bitmap, vsa_stream_t stream) {
+  if (rows < 0 || nb < 1 || max_kv < 1) return VSA_ERR_INVALID_ARG;
+  if (rows == 0) return VSA_OK;
+  if (!q2k_idx || !q2k_num || !bitmap) return VSA_ERR_INVALID_ARG;
+  lut_to_bitmap_kernel<<<rows, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      q2k_idx, q2k_num, max_kv, nb, bitmap);
+  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
+}
+
+vsa_status vsa_bitmap_to_lut(const int8_t* bitmap, int rows, int nb, int max_kv,
+                             int32_t* q2k_idx, int32_t* q2k_num, vsa_stream_t stream) {
+  if (rows < 0 || nb < 1 || max_kv < 1) return VSA_ERR_INVALID_ARG;
+  if (rows == 0) return VSA_OK;
+  if (!bitmap || !q2k_idx || !q2k_num) return VSA_ERR_INVALID_ARG;
+  const int warps = 8;
+  const int grid = (rows + warps - 1) / warps;
+  bitmap_to_lut_kernel<<<grid, warps * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      bitmap, rows, nb, max_kv, q2k_idx, q2k_num);
+  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
+}
+
+vsa_status vsa_fwd_from_host(const vsa_bf16* h_q, const vsa_bf16* h_k, const vsa_bf16* h_v,
+                             const int32_t* h_q2k_idx, const int32_t* h_q2k_num,
+                             const int32_t* h_variable_block_sizes, int B, int H, int S, int D,
+                             int max_kv, int block, float scale, vsa_bf16* h_out, float* h_lse,
+                             vsa_bf16* d_q, vsa_bf16* d_k, vsa_bf16* d_v, int32_t* d_q2k_idx,
+                             int32_t* d_q2k_num, int32_t* d_variable_block_sizes,
+                             vsa_bf16* d_out, float* d_lse, void* workspace,
+                             vsa_stream_t stream) {
+  if (B < 0 || H < 0 || S < 0 || D != VSA_HEAD_DIM || (block != 64 && block != 128) ||
+      S % block != 0 || max_kv < 1)
+    return (D != VSA_HEAD_DIM || (block != 64 && block != 128)) ? VSA_ERR_UNSUPPORTED
+                                                                : VSA_ERR_INVALID_ARG;
+  const size_t rows = (size_t)B * H * S;
+  if (rows == 0) return VSA_OK;
+  if (!h_q || !h_k || !h_v || !h_q2k_idx || !h_q2k_num || !h_variable_block_sizes || !h_out ||
+      (h_lse && !d_lse))
+    return VSA_ERR_INVALID_ARG;
+  const size_t nb = (size_t)S / block;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t tbytes = rows * D * 2;
+  const size_t lut_rows = (size_t)B * H * nb;
+  // validate the device-side arguments before any copy is enqueued
+  DeviceInfo* dev = nullptr;
+  bool nothing = false;
+  vsa_status st = common_checks(d_q, d_k, d_v, d_out, B, H, S, D, block, scale, &dev, &nothing);
+  if (st != VSA_OK) return st;
+  if (!d_q2k_idx || !d_q2k_num || !d_variable_block_sizes) return VSA_ERR_INVALID_ARG;
+  if (cudaMemcpyAsync(d_q, h_q, tbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(d_k, h_k, tbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(d_v, h_v, tbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(d_q2k_idx, h_q2k_idx, lut_rows * max_kv * 4, cudaMemcpyHostToDevice, s) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(d_q2k_num, h_q2k_num, lut_rows * 4, cudaMemcpyHostToDevice, s) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(d_variable_block_sizes, h_variable_block_sizes, nb * 4,
+                      cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  st = vsa_fwd(d_q, d_k, d_v, d_q2k_idx, d_q2k_num, d_variable_block_sizes, B, H, S, D, max_kv,
+               block, scale, d_out, h_lse ? d_lse : nullptr, workspace, stream);
+  if (st != VSA_OK) return st;
+  if (cudaMemcpyAsync(h_out, d_out, tbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  if (h_lse && cudaMemcpyAsync(h_lse, d_lse, rows * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  return VSA_OK;
+}
+
+vsa_status vsa_device_status(vsa_stream_t stream, unsigned int* detail) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof v) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_status, &zero, sizeof zero) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  if (detail) *detail = v;
+  return v == 0 ? VSA_OK : VSA_ERR_DEVICE_TIMEOUT;
+}
+
+int vsa_last_launch_count(void) { return t_last_launches; }
+
+const char* vsa_status_str(vsa_status s) {
+  switch (s) {
+    case VSA_OK: return "ok";
+    case VSA_ERR_INVALID_ARG: return "invalid argument";
+    case VSA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case VSA_ERR_CUDA: return "CUDA runtime error";
+    case VSA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

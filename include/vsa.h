@@ -1,0 +1,169 @@
+/*
+ * vsa.h -- C ABI of the GB300 (sm_103a) block-sparse attention forward library
+ * (libvsa_gb300.so).
+ *
+ * The operation (both entry points compute the same thing; they differ in how the
+ * block selection is encoded):
+ *
+ *   For batch b, head h and query row i, let qb = i / block be its query block.
+ *   Key j (key block kb = j / block) is attended iff kb is selected for (b, h, qb)
+ *   and (j mod block) < variable_block_sizes[kb].  Over the attended keys A_i:
+ *
+ *     out[b,h,i,:] = sum_{j in A_i} softmax_j(scale * q_i . k_j) * v[b,h,j,:]
+ *     lse[b,h,i]   = log2( sum_{j in A_i} exp(scale * q_i . k_j) )
+ *                  = max_j(q_i.k_j * scale * log2 e) + log2(l)      (base 2)
+ *
+ *   A row with no attended key gets out = +0.0 in every element and
+ *   lse = VSA_LSE_EMPTY.
+ *
+ *   Sources: "FastVideo block_sparse_attn_sm100a.py" -- module docstring (forward
+ *   returns (out, lse), lse = max(qk*qk_scale) + log2(l), [B,H,S] fp32; 64- and
+ *   128-token blocks) and is_supported docstring (BHSD bf16, head_dim 128, even
+ *   number of blocks, per-row counts in [0, max_kv], padding past a row's count never
+ *   read, count 0 -> zero output and a finite LSE sentinel, keys at or past a block's
+ *   valid count masked); "TheRock rocke sparse_attention.py" -- module docstring (the
+ *   Jenga i8 MaskBitmap[q_block, k_block], 1 = attend; the VSA per-q-block LUT of
+ *   BlockCount entries) and _lds_bitmap_predicate (a nonzero byte means attend).
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are dense and contiguous.  q, k, v, out are bf16 bit patterns laid out
+ *     [B, H, S, D] (BHSD), D = VSA_HEAD_DIM = 128, 16-byte aligned.  The library
+ *     never takes ownership of and never retains a pointer; it allocates nothing.
+ *   - Device pointers unless the name says host.  All work is enqueued on `stream`
+ *     (a cudaStream_t; NULL = the legacy default stream) and is asynchronous: the
+ *     call returns once the work is enqueued.  No host-device synchronisation, no
+ *     reads of tensor contents on the host.
+ *   - Argument checks happen on the host before anything is enqueued; a failed check
+ *     returns an error and enqueues nothing.
+ *   - Metadata is int32.  LUT entries below a row's count must lie in [0, nb);
+ *     entries outside that range are skipped, counts are clamped to [0, max_kv], and
+ *     a block named twice in one row is attended once (set semantics).
+ *   - Each kernel bounds every internal wait (about one second).  A wait that runs
+ *     out records a code in a device status word and the kernel returns early; read
+ *     it with vsa_device_status().
+ */
+#ifndef VSA_GB300_H
+#define VSA_GB300_H
+
+#include <float.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum vsa_status {
+  VSA_OK = 0,
+  VSA_ERR_INVALID_ARG = 1,    /* null pointer, bad shape, misaligned tensor, bad scale */
+  VSA_ERR_UNSUPPORTED = 2,    /* valid but not built for: D != 128, block not 64/128,
+                                 odd block count, too many blocks, device not sm_103 */
+  VSA_ERR_CUDA = 3,           /* a CUDA runtime call failed (launch, copy, attribute) */
+  VSA_ERR_DEVICE_TIMEOUT = 4  /* a kernel gave up on an internal wait (vsa_device_status) */
+} vsa_status;
+
+/* Finite stand-in for log2(0) written to lse for rows with no attended key:
+ * -FLT_MAX, the most negative finite binary32. */
+#define VSA_LSE_EMPTY (-FLT_MAX)
+#define VSA_HEAD_DIM 128
+/* Largest number of key blocks per sequence (S / block) the kernels accept. */
+#define VSA_MAX_BLOCKS 2048
+
+/* every entry point is exported from the shared library */
+#if defined(__GNUC__)
+#define VSA_API __attribute__((visibility("default")))
+#else
+#define VSA_API
+#endif
+
+typedef uint16_t vsa_bf16;            /* bf16 bit pattern */
+typedef struct CUstream_st *vsa_stream_t; /* == cudaStream_t */
+
+/* VSA forward.
+ *   q, k, v      [B, H, S, D] bf16.
+ *   q2k_idx      [B, H, nb, max_kv] int32, nb = S / block: the key blocks each query
+ *                block attends; row (b, h, qb) holds its q2k_num[b, h, qb] valid entries
+ *                first, anything after them (e.g. -1 padding) is never read.
+ *   q2k_num      [B, H, nb] int32 valid-entry counts (0 allowed).
+ *   variable_block_sizes  [nb] int32, each in [0, block]: valid keys of each key block;
+ *                keys at positions >= it are masked (values are clamped to [0, block]).
+ *   block        64 or 128 tokens per block; S must be a multiple, nb = S / block even.
+ *   scale        natural-exp softmax scale (finite, > 0), typically 1/sqrt(D).
+ *   out          [B, H, S, D] bf16 output; must not overlap any input.
+ *   lse          [B, H, S] fp32 output (base 2), or NULL to skip it (need_lse = false).
+ *   workspace    NULL, or device memory of at least vsa_workspace_bytes() bytes that
+ *                is all zero before the first call; each call leaves it zero again.
+ *                With a workspace, work items are handed out dynamically (better
+ *                balance for uneven counts); calls sharing one workspace must not
+ *                overlap on the GPU.  NULL selects a static round-robin schedule.
+ * Source: "FastVideo block_sparse_attn_sm100a.py", block_sparse_attn_sm100a and
+ * is_supported; "TheRock rocke sparse_attention.py", build_vsa_sparse_attention. */
+VSA_API vsa_status vsa_fwd(const vsa_bf16 *q, const vsa_bf16 *k, const vsa_bf16 *v,
+                   const int32_t *q2k_idx, const int32_t *q2k_num,
+                   const int32_t *variable_block_sizes, int B, int H, int S, int D,
+                   int max_kv, int block, float scale, vsa_bf16 *out, float *lse,
+                   void *workspace, vsa_stream_t stream);
+
+/* Jenga forward: the selection is one i8 bitmap mask_bitmap[S/block_q, S/block_k],
+ * shared by every batch and head; a nonzero byte means attend.  Every key of a selected
+ * block is valid (no tail mask).  block_q == block_k, 64 or 128; S a multiple of it with
+ * an even block count.  Other arguments as vsa_fwd.
+ * Source: "TheRock rocke sparse_attention.py", module docstring (Jenga bullet),
+ * _stage_jenga_mask_to_lds, _lds_bitmap_predicate, build_jenga_sparse_attention. */
+VSA_API vsa_status jenga_fwd(const vsa_bf16 *q, const vsa_bf16 *k, const vsa_bf16 *v,
+                     const int8_t *mask_bitmap, int B, int H, int S, int D, int block_q,
+                     int block_k, float scale, vsa_bf16 *out, float *lse, void *workspace,
+                     vsa_stream_t stream);
+
+/* Bytes of device workspace vsa_fwd / jenga_fwd use when given one. */
+VSA_API size_t vsa_workspace_bytes(void);
+
+/* LUT -> bitmap, bit-exact: bitmap[r, kb] = 1 iff kb is one of the first
+ * clamp(q2k_num[r], 0, max_kv) entries of q2k_idx row r (entries outside [0, nb)
+ * skipped), else 0.  q2k_idx [rows, max_kv], q2k_num [rows], bitmap [rows, nb] int8.
+ * Source: "TheRock rocke sparse_attention.py", _stage_vsa_bitmap_to_lds (zero the
+ * row, then scatter 1 at every listed block; idempotent). */
+VSA_API vsa_status vsa_lut_to_bitmap(const int32_t *q2k_idx, const int32_t *q2k_num, int rows,
+                             int max_kv, int nb, int8_t *bitmap, vsa_stream_t stream);
+
+/* bitmap -> LUT, bit-exact: row r lists the indices of its nonzero bytes in
+ * ascending order, the first min(count, max_kv) of them, then -1 up to max_kv;
+ * q2k_num[r] = min(count, max_kv).  bitmap [rows, nb] int8 -> q2k_idx [rows, max_kv],
+ * q2k_num [rows] int32.
+ * Source: "FastVideo block_sparse_attn_sm100a.py", _block_sparse_attn_sm100a_from_
+ * mask_inference (a bool block map compacted into (q2k_idx, q2k_num), -1 fill). */
+VSA_API vsa_status vsa_bitmap_to_lut(const int8_t *bitmap, int rows, int nb, int max_kv,
+                             int32_t *q2k_idx, int32_t *q2k_num, vsa_stream_t stream);
+
+/* vsa_fwd with HOST buffers: copies q, k, v, q2k_idx, q2k_num, variable_block_sizes
+ * from host memory into the caller's device buffers (the d_* arguments, same shapes as
+ * vsa_fwd), runs vsa_fwd, and copies out (and lse, if h_lse is not NULL) back to host
+ * memory, all enqueued on `stream`.  The caller synchronises the stream before reading
+ * h_out / h_lse.  Host buffers should be pinned (page-locked) for the copies to be
+ * asynchronous.  d_lse may be NULL only if h_lse is NULL. */
+VSA_API vsa_status vsa_fwd_from_host(const vsa_bf16 *h_q, const vsa_bf16 *h_k, const vsa_bf16 *h_v,
+                             const int32_t *h_q2k_idx, const int32_t *h_q2k_num,
+                             const int32_t *h_variable_block_sizes, int B, int H, int S,
+                             int D, int max_kv, int block, float scale, vsa_bf16 *h_out,
+                             float *h_lse, vsa_bf16 *d_q, vsa_bf16 *d_k, vsa_bf16 *d_v,
+                             int32_t *d_q2k_idx, int32_t *d_q2k_num,
+                             int32_t *d_variable_block_sizes, vsa_bf16 *d_out, float *d_lse,
+                             void *workspace, vsa_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the device status word of the current
+ * device: VSA_OK, or VSA_ERR_DEVICE_TIMEOUT if a kernel gave up on a wait since the
+ * last call (`detail`, if not NULL, receives the recorded code). */
+VSA_API vsa_status vsa_device_status(vsa_stream_t stream, unsigned int *detail);
+
+/* Number of kernel launches the most recent successful vsa_fwd / jenga_fwd call on
+ * this thread enqueued (for accounting in benchmarks). */
+VSA_API int vsa_last_launch_count(void);
+
+/* Static text for a status code. */
+VSA_API const char *vsa_status_str(vsa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VSA_GB300_H */

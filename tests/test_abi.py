@@ -1,0 +1,99 @@
+"""The C-ABI library loads and exports every entry point include/vsa.h declares; host-side
+argument checks reject bad calls with the documented status before touching the GPU.
+Runs without a GPU (no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_sparse_attention_vsa_gb300 import binding
+from block_sparse_attention_vsa_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vsa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vsa_\w+|jenga_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return binding.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("vsa_fwd", "jenga_fwd", "vsa_lut_to_bitmap", "vsa_bitmap_to_lut"):
+        assert n in names
+    assert set(names) == set(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_library_has_sm103a_code_only():
+    # the build passes exactly one -gencode, for sm_103a
+    assert libbuild.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.vsa_status_str(code)
+
+
+NULL = None
+
+
+def _fwd(lib, **kw):
+    args = dict(q=1 << 20, k=2 << 20, v=3 << 20, idx=4 << 20, num=5 << 20, vbs=6 << 20, B=1, H=1,
+                S=256, D=128, max_kv=4, block=64, scale=0.088, out=7 << 20, lse=None, ws=None)
+    args.update(kw)
+    P = ctypes.c_void_p
+    return lib.vsa_fwd(P(args["q"]), P(args["k"]), P(args["v"]), P(args["idx"]), P(args["num"]),
+                       P(args["vbs"]), args["B"], args["H"], args["S"], args["D"], args["max_kv"],
+                       args["block"], args["scale"], P(args["out"]),
+                       P(args["lse"]) if args["lse"] else None,
+                       P(args["ws"]) if args["ws"] else None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=64), binding.VSA_ERR_UNSUPPORTED),
+    (dict(block=32), binding.VSA_ERR_UNSUPPORTED),
+    (dict(S=64 * 3), binding.VSA_ERR_UNSUPPORTED),        # odd number of blocks
+    (dict(S=100), binding.VSA_ERR_INVALID_ARG),           # not a multiple of the block
+    (dict(S=64 * 4096), binding.VSA_ERR_UNSUPPORTED),     # more than VSA_MAX_BLOCKS blocks
+    (dict(scale=0.0), binding.VSA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.VSA_ERR_INVALID_ARG),
+    (dict(B=-1), binding.VSA_ERR_INVALID_ARG),
+])
+def test_host_validation_without_gpu(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+
+
+def test_empty_problem_is_a_no_op(lib):
+    assert _fwd(lib, B=0) == binding.VSA_OK
+    assert _fwd(lib, S=0) == binding.VSA_OK
+
+
+def test_jenga_requires_square_blocks(lib):
+    P = ctypes.c_void_p
+    code = lib.jenga_fwd(P(1 << 20), P(2 << 20), P(3 << 20), P(4 << 20), 1, 1, 256, 128, 64, 128,
+                         0.088, P(5 << 20), None, None, None)
+    assert code == binding.VSA_ERR_UNSUPPORTED
+
+
+def test_metadata_validation(lib):
+    P = ctypes.c_void_p
+    assert lib.vsa_lut_to_bitmap(P(1 << 20), P(2 << 20), -1, 4, 8, P(3 << 20), None) == \
+        binding.VSA_ERR_INVALID_ARG
+    assert lib.vsa_lut_to_bitmap(P(1 << 20), P(2 << 20), 0, 4, 8, P(3 << 20), None) == binding.VSA_OK
+    assert lib.vsa_bitmap_to_lut(P(1 << 20), 4, 8, 0, P(2 << 20), P(3 << 20), None) == \
+        binding.VSA_ERR_INVALID_ARG
+    assert lib.vsa_workspace_bytes() >= 8
