@@ -386,17 +386,19 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, int lim0, int lim1, in
     m_run = m_tile;
   }
   const float neg = (m_run == -INFINITY) ? 0.0f : -m_run;
+#pragma unroll
+  for (int j = 0; j < NK; ++j) s[j] = fast_exp2(fmaf(s[j], sl2, neg));
+  // P is rounded to bf16 for the PV MMA; l sums exactly those rounded weights, so the
+  // weights applied to V are normalised consistently (with a lagging reference max the
+  // unrounded sum would leave up to ~2^-8 relative mismatch on dominant keys).
+  uint32_t pk[NK / 2];
   float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < NK; ++j) {
-    const float p = fast_exp2(fmaf(s[j], sl2, neg));
-    sum[j & 3] += p;
-    s[j] = p;
+  for (int i = 0; i < NK / 2; ++i) {
+    pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
+    sum[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
   }
   l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
-  uint32_t pk[NK / 2];
-#pragma unroll
-  for (int i = 0; i < NK / 2; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
 #pragma unroll
   for (int c = 0; c < NK / 64; ++c)
     tmem_st_32x32b_x32(tS + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[c * 32]));
