@@ -74,6 +74,7 @@ struct DeviceInfo {
   int sm_count = 0;
   int major = 0, minor = 0;
   bool attr_set[4] = {false, false, false, false};
+  int regs[4] = {0, 0, 0, 0};
 };
 std::mutex g_mu;
 DeviceInfo g_dev[64];
@@ -139,14 +140,21 @@ vsa_status launch_fwd(DeviceInfo* dev, int slot, const void* q, const void* k, c
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kSmemBytes) != cudaSuccess)
         return VSA_ERR_CUDA;
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return VSA_ERR_CUDA;
+      dev->regs[slot] = fa.numRegs;
       dev->attr_set[slot] = true;
     }
   }
+  // The kernel moves registers between warpgroups (setmaxnreg); the launch must provide
+  // the pool that re-balancing draws on, or a warpgroup would wait for registers forever.
+  if ((long long)dev->regs[slot] * kThreads < (long long)kRegPoolNeeded) return VSA_ERR_UNSUPPORTED;
   CUtensorMap tq, tk, tv, to;
   if (!make_map(&tq, q, rows, 128) || !make_map(&tk, k, rows, BLOCK) ||
       !make_map(&tv, v, rows, BLOCK) || !make_map(&to, out, rows, 128))
     return VSA_ERR_CUDA;
-  const int grid = args.n_items < dev->sm_count ? args.n_items : dev->sm_count;
+  const int ctas = (args.n_items + 1) / 2;  // two work items in flight per CTA
+  const int grid = ctas < dev->sm_count ? ctas : dev->sm_count;
   kern<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, args);
   if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
   t_last_launches = 1;

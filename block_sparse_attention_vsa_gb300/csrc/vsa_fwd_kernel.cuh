@@ -7,25 +7,6 @@
 // block_sparse_attn_sm100a.py", module and is_supported docstrings; "TheRock rocke
 // sparse_attention.py", module docstring and the two build_* kernels.)
 //
-// How (one persistent CTA per SM, 10 warps, warp-specialised):
-//   warp 8        producer: per work item, turns the LUT rows (or the Jenga bitmap
-//                 rows) into an ascending list of selected key blocks in shared memory
-//                 -- an SMEM bitmap scatter followed by a ballot/popc compaction, so a
-//                 repeated or out-of-range LUT entry can never cause a duplicate or an
-//                 out-of-bounds copy -- then issues TMA copies of Q and of ONLY the
-//                 selected K/V blocks into a 4-stage ring (mbarrier full/empty pairs).
-//   warp 9        MMA issuer: S = Q K^T (both operands from SMEM) into a
-//                 double-buffered TMEM S tile, then O += P V with P read from TMEM
-//                 (P overwrites S in place as bf16) and O in a double-buffered TMEM
-//                 accumulator.
-//   warps 0-3     softmax: one thread per query row; loads its S row from TMEM,
-//                 applies the tail-key / row-half mask, keeps a running max in the
-//                 log2 domain and only rescales O and l when the max grows by more
-//                 than 2^8 (the reference value may lag the true max; out = O/l and
-//                 lse = m + log2 l are exact for any common reference), writes bf16 P.
-//   warps 4-7     epilogue: out = O / l (or +0 for empty rows) staged in SMEM and
-//                 written by a TMA store; lse = m + log2 l or the sentinel.
-//
 // Work item = 128 query rows (the M of one tcgen05 MMA):
 //   block 128: one query block; one key tile = one selected key block (N = 128).
 //   block 64 : an adjacent PAIR of query blocks (the pairing "FastVideo
@@ -34,6 +15,29 @@
 //              each union entry carries a 2-bit row-half mask, and rows of the query
 //              block that did not select it see -inf.  Two union blocks form one key
 //              tile (N = 128; the last tile of an odd union has N = 64).
+//
+// Structure: one persistent CTA per SM, 12 warps.
+//   warp 8      producer: per work item, turns the LUT rows (or Jenga bitmap rows) into
+//               an ascending list of selected key blocks -- an SMEM byte-map scatter then
+//               a ballot/popc compaction, so repeated or out-of-range LUT entries can
+//               never cause a duplicate or an out-of-bounds copy -- then TMA-loads Q
+//               (double-buffered across items) and ONLY the selected K/V blocks into a
+//               4-stage ring, in the order the MMA warp consumes them.
+//   warp 9      MMA issuer (one thread): S_t = Q K_t^T into TMEM S buffer t%2, then
+//               O_{t%2} += P_t V_t with P_t read from TMEM.  Issue order per item:
+//               QK0, QK1, PV0, QK2, PV1, ..., so QK_{t+1} runs while P_t is computed.
+//   warps 0-3   softmax warpgroup 0: the item's even key tiles;
+//   warps 4-7   softmax warpgroup 1: the item's odd key tiles.  One thread per query
+//               row; each warpgroup keeps its own running max m (log2 domain, allowed to
+//               lag the true max by up to 2^8 before O and l are rescaled), row sums and
+//               O accumulator, so the two never synchronise inside the key loop.
+//               After the item they merge (m, l, O) of both halves and each warpgroup
+//               normalises, stages and TMA-stores one 64-column half of the output;
+//               warpgroup 0 writes lse.
+//   warps 10-11 idle.
+// TMEM (512 columns): S0, S1 at columns 0, 128; O0, O1 at 256, 384.
+// Every mbarrier wait is bounded; a wait that runs out records a code in the device
+// status word, raises the CTA's abort flag and every role returns.
 #pragma once
 
 #include <cuda.h>
@@ -43,46 +47,47 @@
 
 namespace vsa {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kStages = 4;
 constexpr int kMaxNb = 2048;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per wait
 constexpr float kRescaleThreshold = 8.0f;         // log2 units: stale max allowed to lag 2^8
+constexpr uint32_t kSoftmaxRegs = 216;            // per thread, softmax warpgroups
+constexpr uint32_t kOtherRegs = 56;               // per thread, producer/MMA warpgroup
+// registers the launch must provide for the re-balancing above (checked on the host)
+constexpr uint32_t kRegPoolNeeded = 256 * kSoftmaxRegs + 128 * kOtherRegs;
 
 // shared-memory map (bytes from a 1024-aligned base)
-constexpr uint32_t kQBytes = 128 * 128 * 2;      // one Q (or out staging) tile
-constexpr uint32_t kTileBytes = 128 * 128 * 2;   // one K or V tile of up to 128 keys
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffKV = kOffQ + 2 * kQBytes;
-constexpr uint32_t kOffList = kOffKV + kStages * kTileBytes;
-constexpr uint32_t kOffBm = kOffList + 2 * kMaxNb * 4;
-constexpr uint32_t kOffStats = kOffBm + 2 * kMaxNb;
-constexpr uint32_t kOffCtl = kOffStats + 2 * 2 * 128 * 4;
+constexpr uint32_t kTileBytes = 128 * 128 * 2;  // a Q / out-staging / K / V tile
+constexpr uint32_t kOffQ = 0;                   // Q[2] (double-buffered across items)
+constexpr uint32_t kOffKV = 2 * kTileBytes;     // K/V ring [kStages]
+constexpr uint32_t kOffList = kOffKV + kStages * kTileBytes;  // list[2][kMaxNb] u32
+constexpr uint32_t kOffBm = kOffList + 2 * kMaxNb * 4;       // byte maps [2][kMaxNb]
+constexpr uint32_t kOffStats = kOffBm + 2 * kMaxNb;          // [item parity][wg][3][128] f32
+constexpr uint32_t kStatsBytes = 2 * 2 * 3 * 128 * 4;
+constexpr uint32_t kOffCtl = kOffStats + kStatsBytes;
 constexpr uint32_t kCtlBytes = 1024;
 constexpr uint32_t kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + alignment slack
 
-// TMEM columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // two S/P buffers of 128 columns
-constexpr uint32_t kColO = 256;  // two O buffers of 128 columns
+constexpr uint32_t kColS = 0;    // S0, S1
+constexpr uint32_t kColO = 256;  // O0, O1
 
-// device status codes (the low byte names the wait that gave up)
-constexpr unsigned kErrTimeout = 0x100u;
+constexpr unsigned kErrTimeout = 0x100u;  // | code of the wait that gave up
 
 struct SmemCtl {
+  uint64_t list_full[2], list_empty[2];
   uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t list_full[2], list_empty[2];
   uint64_t s_full[2], p_full[2];
-  uint64_t pv_done;
-  uint64_t o_full[2], o_empty[2];
-  uint64_t stats_full[2];
+  uint64_t o_full, o_empty;
+  uint64_t stats_bar[2];
   uint64_t epi_bar[2];
   uint64_t drain;
+  int hdr_item[2];
+  int hdr_n[2];  // list entries of the item
   uint32_t tmem_base;
   int abort_flag;
-  int hdr_item[2];
-  int hdr_n[2];
 };
 static_assert(sizeof(SmemCtl) <= kCtlBytes, "control block too large");
 
@@ -100,8 +105,8 @@ struct FwdArgs {
 
 // Bounded wait on an mbarrier phase.  Gives up after kWaitLimitNs (recording `code` in
 // the device status word and raising the CTA's abort flag), or as soon as another role
-// has raised the abort flag (unless `drain`: waits for copies / MMAs in flight still run
-// to their own time limit so nothing is in flight when the CTA exits).
+// has raised the abort flag -- unless `drain`: a wait for copies / MMAs still in flight
+// runs to its own time limit, so nothing is in flight when the CTA exits.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, SmemCtl* ctl,
                                          unsigned* status, unsigned code, bool drain = false) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -121,11 +126,15 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, SmemCtl
 __device__ __forceinline__ uint32_t make_entry(int kb, uint32_t halves, int valid) {
   return (uint32_t)kb | (halves << 16) | ((uint32_t)valid << 20);
 }
+// valid keys of an entry for a row in query half `half` (0 if that half did not select it)
+__device__ __forceinline__ int entry_limit(uint32_t e, uint32_t half) {
+  return ((e >> (16 + half)) & 1u) ? (int)((e >> 20) & 0xFFu) : 0;
+}
 
-template <int BLOCK, bool JENGA>
+template <int BLOCK>
 struct Cfg {
-  static constexpr int kSub = (BLOCK == 64) ? 2 : 1;     // key blocks per key tile
-  static constexpr int kPairs = (BLOCK == 64) ? 2 : 1;   // query blocks per work item
+  static constexpr int kSub = (BLOCK == 64) ? 2 : 1;    // key blocks per key tile
+  static constexpr int kPairs = (BLOCK == 64) ? 2 : 1;  // query blocks per work item
 };
 
 // ------------------------------------------------------------------------------------
@@ -135,19 +144,19 @@ template <int BLOCK, bool JENGA>
 __device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
                               const CUtensorMap* tq, const CUtensorMap* tk,
                               const CUtensorMap* tv) {
-  using C = Cfg<BLOCK, JENGA>;
+  using C = Cfg<BLOCK>;
   const uint32_t lane = lane_id();
   uint8_t* bm0 = smem + kOffBm;
   uint8_t* bm1 = bm0 + kMaxNb;
   const uint64_t pol_kv = policy_evict_last();
   const uint64_t pol_q = policy_evict_first();
-  uint32_t L = 0;  // K/V tiles loaded so far (ring position)
-  uint32_t fills[kStages] = {0, 0, 0, 0};
-  uint32_t qfills[2] = {0, 0};
   const int nb = a.nb;
-  for (uint32_t it = 0;; ++it) {
+  uint32_t L = 0;                            // K/V tiles loaded so far (ring position)
+  uint32_t fills[kStages] = {0, 0, 0, 0};    // copies issued per ring stage
+  uint32_t qfills[2] = {0, 0};               // Q copies issued per Q buffer
+  bool ok = true;
+  for (uint32_t it = 0; ok; ++it) {
     const uint32_t buf = it & 1;
-    // ---- next work item
     int item;
     if (a.sched == nullptr) {
       const long long s = (long long)blockIdx.x + (long long)it * gridDim.x;
@@ -160,14 +169,12 @@ __device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
     }
     if (it >= 2 && !wait_bar(&ctl->list_empty[buf], ((it >> 1) + 1) & 1, ctl, a.status, 1)) break;
     uint32_t* list = reinterpret_cast<uint32_t*>(smem + kOffList) + buf * kMaxNb;
-    int count = 0;
-    int bh = 0, qa = 0;
+    int count = 0, bh = 0, qa = 0;
     if (item >= 0) {
       const int items_per_bh = nb / C::kPairs;
       bh = item / items_per_bh;
       qa = (item - bh * items_per_bh) * C::kPairs;
       if (!JENGA) {
-        // scatter the LUT rows of the item's query blocks into per-half byte maps
 #pragma unroll
         for (int hf = 0; hf < C::kPairs; ++hf) {
           const long long row = (long long)bh * nb + qa + hf;
@@ -182,7 +189,6 @@ __device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
         }
         __syncwarp();
       }
-      // ascending compaction of the selected blocks
       for (int base = 0; base < nb; base += 32) {
         const int kb = base + (int)lane;
         uint32_t h0 = 0, h1 = 0;
@@ -204,8 +210,7 @@ __device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
             valid = a.vbs[kb];
             valid = valid < 0 ? 0 : (valid > BLOCK ? BLOCK : valid);
           }
-          const uint32_t halves = (C::kPairs == 2) ? (h0 | (h1 << 1)) : 3u;
-          list[pos] = make_entry(kb, halves, valid);
+          list[pos] = make_entry(kb, (C::kPairs == 2) ? (h0 | (h1 << 1)) : 3u, valid);
           if (!JENGA) {
             bm0[kb] = 0;
             if (C::kPairs == 2) bm1[kb] = 0;
@@ -222,21 +227,19 @@ __device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
     }
     __syncwarp();
     if (item < 0) break;
-
-    // ---- Q tile (128 rows) of the item
-    const int row0 = bh * a.S + qa * BLOCK;
+    // Q (also the item's output staging buffer): free once the item two back is stored
     if (it >= 2 && !wait_bar(&ctl->q_empty[buf], ((it >> 1) + 1) & 1, ctl, a.status, 2)) break;
-    uint8_t* qs = smem + kOffQ + buf * kQBytes;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&ctl->q_full[buf], kQBytes);
-      tma_load_2d_hint(qs, tq, &ctl->q_full[buf], 0, row0, pol_q);
-      tma_load_2d_hint(qs + kQBytes / 2, tq, &ctl->q_full[buf], 64, row0, pol_q);
-    }
-    qfills[buf]++;
-
-    // ---- K/V tiles in the order the MMA warp consumes them: K0, K1, V0, K2, V1, ...
     const int n_tiles = (count + C::kSub - 1) / C::kSub;
-    bool ok = true;
+    if (n_tiles == 0) continue;
+    const int row0 = bh * a.S + qa * BLOCK;
+    uint8_t* qs = smem + kOffQ + buf * kTileBytes;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&ctl->q_full[buf], kTileBytes);
+      tma_load_2d_hint(qs, tq, &ctl->q_full[buf], 0, row0, pol_q);
+      tma_load_2d_hint(qs + kTileBytes / 2, tq, &ctl->q_full[buf], 64, row0, pol_q);
+    }
+    ++qfills[buf];
+    // K/V tiles in the order the MMA warp consumes them: K0, K1, V0, K2, V1, ...
     for (int t = 0; t <= n_tiles && ok; ++t) {
 #pragma unroll
       for (int which = 0; which < 2; ++which) {  // 0: K of tile t, 1: V of tile t-1
@@ -255,19 +258,17 @@ __device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
         if (lane == 0) {
           mbar_arrive_expect_tx(&ctl->kv_full[stage], (uint32_t)ne * BLOCK * 128 * 2);
           for (int e = 0; e < ne; ++e) {
-            const int kb = (int)(list[e0 + e] & 0xFFFFu);
-            const int krow = bh * a.S + kb * BLOCK;
+            const int krow = bh * a.S + (int)(list[e0 + e] & 0xFFFFu) * BLOCK;
             // d-halves are separate [128 rows][64] sub-tiles; block e fills rows e*BLOCK..
             tma_load_2d_hint(dst + e * BLOCK * 128, map, &ctl->kv_full[stage], 0, krow, pol_kv);
             tma_load_2d_hint(dst + kTileBytes / 2 + e * BLOCK * 128, map, &ctl->kv_full[stage],
                              64, krow, pol_kv);
           }
         }
-        fills[stage]++;
+        ++fills[stage];
         ++L;
       }
     }
-    if (!ok) break;
   }
   // drain: every copy this warp issued has landed before the CTA can exit
   for (int s = 0; s < kStages; ++s)
@@ -281,11 +282,14 @@ __device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
 // ------------------------------------------------------------------------------------
 template <int BLOCK, bool JENGA>
 __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t tmem) {
-  using C = Cfg<BLOCK, JENGA>;
+  using C = Cfg<BLOCK>;
   constexpr uint32_t kIdescS128 = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t kIdescS64 = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);
-  uint32_t L = 0, g = 0;
+  uint32_t L = 0;            // ring position
+  uint32_t gt[2] = {0, 0};   // tiles issued per softmax warpgroup (S buffer / P phases)
+  uint32_t ne_items = 0;     // non-empty items so far (O phases)
+  uint32_t nq[2] = {0, 0};   // Q fills consumed per Q buffer
   for (uint32_t it = 0;; ++it) {
     const uint32_t buf = it & 1;
     if (!wait_bar(&ctl->list_full[buf], (it >> 1) & 1, ctl, a.status, 10)) break;
@@ -293,23 +297,26 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
     const int count = ctl->hdr_n[buf];
     mbar_arrive(&ctl->list_empty[buf]);
     if (item < 0) break;
-    if (it >= 2 && !wait_bar(&ctl->o_empty[buf], ((it >> 1) + 1) & 1, ctl, a.status, 11)) break;
-    if (!wait_bar(&ctl->q_full[buf], (it >> 1) & 1, ctl, a.status, 12)) break;
-    tc_fence_after();
-    const uint32_t qaddr = smem_addr(smem + kOffQ + buf * kQBytes);
-    const uint32_t tO = tmem + kColO + buf * 128;
     const int n_tiles = (count + C::kSub - 1) / C::kSub;
+    if (n_tiles == 0) continue;
+    if (!wait_bar(&ctl->q_full[buf], nq[buf] & 1, ctl, a.status, 11)) break;
+    ++nq[buf];
+    tc_fence_after();
+    const uint32_t qaddr = smem_addr(smem + kOffQ + buf * kTileBytes);
     bool ok = true;
     for (int t = 0; t <= n_tiles && ok; ++t) {
-      if (t < n_tiles) {  // S_t = Q K_t^T
-        const uint32_t gg = g + t;
+      if (t < n_tiles) {  // S_t = Q K_t^T into S buffer t%2
+        const int w = t & 1;
         const uint32_t stage = L % kStages;
-        if (!wait_bar(&ctl->kv_full[stage], (L / kStages) & 1, ctl, a.status, 13)) { ok = false; break; }
+        if (!wait_bar(&ctl->kv_full[stage], (L / kStages) & 1, ctl, a.status, 12)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const int ne = (count - t * C::kSub) < C::kSub ? (count - t * C::kSub) : C::kSub;
         const uint32_t idesc = (ne * BLOCK == 128) ? kIdescS128 : kIdescS64;
         const uint32_t kaddr = smem_addr(smem + kOffKV + stage * kTileBytes);
-        const uint32_t tS = tmem + kColS + (gg & 1) * 128;
+        const uint32_t tS = tmem + kColS + w * 128;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = (k >> 2) * (kTileBytes / 2) + (k & 3) * 32;
@@ -317,32 +324,44 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
                  idesc, k > 0);
         }
         mma_commit(&ctl->kv_empty[stage]);
-        mma_commit(&ctl->s_full[gg & 1]);
+        mma_commit(&ctl->s_full[w]);
         ++L;
       }
-      if (t >= 1) {  // O += P_{t-1} V_{t-1}
+      if (t >= 1) {  // O_{w} += P_{t-1} V_{t-1}
         const int tp = t - 1;
-        const uint32_t gg = g + tp;
-        if (!wait_bar(&ctl->p_full[gg & 1], (gg >> 1) & 1, ctl, a.status, 14)) { ok = false; break; }
+        const int w = tp & 1;
+        if (tp == 0 && ne_items >= 1 &&
+            !wait_bar(&ctl->o_empty, (ne_items - 1) & 1, ctl, a.status, 13)) {
+          ok = false;
+          break;
+        }
+        if (!wait_bar(&ctl->p_full[w], gt[w] & 1, ctl, a.status, 14)) {
+          ok = false;
+          break;
+        }
         const uint32_t stage = L % kStages;
-        if (!wait_bar(&ctl->kv_full[stage], (L / kStages) & 1, ctl, a.status, 15)) { ok = false; break; }
+        if (!wait_bar(&ctl->kv_full[stage], (L / kStages) & 1, ctl, a.status, 15)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const int ne = (count - tp * C::kSub) < C::kSub ? (count - tp * C::kSub) : C::kSub;
         const int ksteps = ne * BLOCK / 16;
         const uint32_t vaddr = smem_addr(smem + kOffKV + stage * kTileBytes);
-        const uint32_t tP = tmem + kColS + (gg & 1) * 128;
+        const uint32_t tP = tmem + kColS + w * 128;
+        const uint32_t tO = tmem + kColO + w * 128;
         for (int k = 0; k < ksteps; ++k) {
           mma_ts(tO, tP + k * 8, smem_desc_sw128(vaddr + k * 2048, kTileBytes / 2, 1024), kIdescPV,
-                 (tp > 0 || k > 0) ? 1u : 0u);
+                 (tp >= 2 || k > 0) ? 1u : 0u);
         }
         mma_commit(&ctl->kv_empty[stage]);
-        mma_commit(&ctl->pv_done);
+        ++gt[w];
         ++L;
       }
     }
     if (!ok) break;
-    mma_commit(&ctl->o_full[buf]);
-    g += n_tiles;
+    mma_commit(&ctl->o_full);
+    ++ne_items;
   }
   // every MMA issued has completed before TMEM can be released
   mma_commit(&ctl->drain);
@@ -350,11 +369,16 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
 }
 
 // ------------------------------------------------------------------------------------
-// softmax warpgroup (warps 0-3): thread = query row of the 128-row tile
+// softmax warpgroups: thread = query row of the 128-row tile
 // ------------------------------------------------------------------------------------
+// One key tile for this row: mask, running max, exp2, both row sums, bf16 P written over
+// S in TMEM.  l_exact sums the fp32 weights (for lse); l_round sums the bf16-rounded
+// weights the PV MMA actually applies (for normalising out), so the weights on V add up
+// to one even when the reference max lags the true one.
 template <int NK>
 __device__ __forceinline__ void softmax_tile(uint32_t tS, int lim0, int lim1, int kps, float sl2,
-                                             float& m_run, float& l_run, float& alpha) {
+                                             float& m_run, float& l_exact, float& l_round,
+                                             float& alpha) {
   uint32_t r[NK];
 #pragma unroll
   for (int c = 0; c < NK / 32; ++c)
@@ -371,14 +395,14 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, int lim0, int lim1, in
       if (jj >= lim) s[j] = -INFINITY;
     }
   }
-  // row max (pairwise tree for ILP)
-  float mx[8];
+  float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-  for (int i = 0; i < 8; ++i) mx[i] = s[i];
+  for (int j = 4; j + 1 < NK; j += 8) {
 #pragma unroll
-  for (int j = 8; j < NK; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
-  const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                           fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+    for (int c = 0; c < 4 && j + 2 * c + 1 < NK; ++c)
+      mx[c] = fmax3(mx[c], s[j + 2 * c], s[j + 2 * c + 1]);
+  }
+  const float mraw = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
   const float m_tile = mraw * sl2;
   alpha = 1.0f;
   if (m_tile > m_run + kRescaleThreshold) {
@@ -386,35 +410,45 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, int lim0, int lim1, in
     m_run = m_tile;
   }
   const float neg = (m_run == -INFINITY) ? 0.0f : -m_run;
-#pragma unroll
-  for (int j = 0; j < NK; ++j) s[j] = fast_exp2(fmaf(s[j], sl2, neg));
-  // P is rounded to bf16 for the PV MMA; l sums exactly those rounded weights, so the
-  // weights applied to V are normalised consistently (with a lagging reference max the
-  // unrounded sum would leave up to ~2^-8 relative mismatch on dominant keys).
+  const uint64_t sl2x2 = f32x2(sl2, sl2), negx2 = f32x2(neg, neg);
+  uint64_t acc_e[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+  uint64_t acc_r[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
   uint32_t pk[NK / 2];
-  float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < NK / 2; ++i) {
-    pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
-    sum[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+    float y0, y1;
+    split_f32x2(fma_f32x2(f32x2(s[2 * i], s[2 * i + 1]), sl2x2, negx2), y0, y1);
+    const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+    acc_e[i & 1] = add_f32x2(acc_e[i & 1], f32x2(p0, p1));
+    pk[i] = pack_bf16x2(p0, p1);
+    acc_r[i & 1] = add_f32x2(acc_r[i & 1], bf16x2_to_f32x2(pk[i]));
   }
-  l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+  float e0, e1, e2, e3, r0, r1, r2, r3;
+  split_f32x2(acc_e[0], e0, e1);
+  split_f32x2(acc_e[1], e2, e3);
+  split_f32x2(acc_r[0], r0, r1);
+  split_f32x2(acc_r[1], r2, r3);
+  l_exact = l_exact * alpha + ((e0 + e1) + (e2 + e3));
+  l_round = l_round * alpha + ((r0 + r1) + (r2 + r3));
 #pragma unroll
   for (int c = 0; c < NK / 64; ++c)
     tmem_st_32x32b_x32(tS + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[c * 32]));
 }
 
 template <int BLOCK, bool JENGA>
-__device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t tmem) {
-  using C = Cfg<BLOCK, JENGA>;
+__device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t tmem,
+                             int w, const CUtensorMap* to) {
+  using C = Cfg<BLOCK>;
   constexpr int kps = BLOCK;  // keys per key block
-  const int row = threadIdx.x;             // 0..127
-  const uint32_t warp = threadIdx.x >> 5;  // 0..3
-  const uint32_t lane_base = (warp * 32) << 16;
+  const int row = threadIdx.x & 127;
+  const uint32_t lane_base = (((threadIdx.x >> 5) & 3) * 32) << 16;  // warp's TMEM lanes
   const uint32_t half = (BLOCK == 64) ? (uint32_t)(row >> 6) : 0u;
-  float* stat_m = reinterpret_cast<float*>(smem + kOffStats);
-  float* stat_l = stat_m + 2 * 128;
-  uint32_t g = 0;
+  const uint32_t tS = tmem + kColS + w * 128 + lane_base;
+  const uint32_t tO0 = tmem + kColO + lane_base, tO1 = tO0 + 128;
+  const uint32_t tOw = w ? tO1 : tO0;
+  float* stats = reinterpret_cast<float*>(smem + kOffStats);  // [par][wg][3][128]
+  const bool leader = row == 0;
+  uint32_t gw = 0, ne_items = 0;
   for (uint32_t it = 0;; ++it) {
     const uint32_t buf = it & 1;
     if (!wait_bar(&ctl->list_full[buf], (it >> 1) & 1, ctl, a.status, 20)) break;
@@ -422,133 +456,127 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
     const int count = ctl->hdr_n[buf];
     if (item < 0) break;
     const uint32_t* list = reinterpret_cast<const uint32_t*>(smem + kOffList) + buf * kMaxNb;
-    const uint32_t tO = tmem + kColO + buf * 128 + lane_base;
     const int n_tiles = (count + C::kSub - 1) / C::kSub;
-    float m_run = -INFINITY, l_run = 0.0f;
+    float m_run = -INFINITY, l_exact = 0.0f, l_round = 0.0f;
     bool ok = true;
-    for (int t = 0; t < n_tiles; ++t) {
-      const uint32_t gg = g + t;
+    for (int t = w; t < n_tiles; t += 2, ++gw) {
       const int e0 = t * C::kSub;
       const int ne = (count - e0) < C::kSub ? (count - e0) : C::kSub;
-      const uint32_t en0 = list[e0];
-      const int lim0 = ((en0 >> (16 + half)) & 1u) ? (int)((en0 >> 20) & 0xFFu) : 0;
-      int lim1 = kps;
-      if (ne > 1) {
-        const uint32_t en1 = list[e0 + 1];
-        lim1 = ((en1 >> (16 + half)) & 1u) ? (int)((en1 >> 20) & 0xFFu) : 0;
+      const int lim0 = entry_limit(list[e0], half);
+      const int lim1 = ne > 1 ? entry_limit(list[e0 + 1], half) : kps;
+      if (!wait_bar(&ctl->s_full[w], gw & 1, ctl, a.status, 21)) {
+        ok = false;
+        break;
       }
-      if (!wait_bar(&ctl->s_full[gg & 1], (gg >> 1) & 1, ctl, a.status, 21)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t tS = tmem + kColS + (gg & 1) * 128 + lane_base;
       float alpha;
       if (ne * BLOCK == 128)
-        softmax_tile<128>(tS, lim0, lim1, kps, a.scale_log2, m_run, l_run, alpha);
+        softmax_tile<128>(tS, lim0, lim1, kps, a.scale_log2, m_run, l_exact, l_round, alpha);
       else
-        softmax_tile<64>(tS, lim0, lim1, kps, a.scale_log2, m_run, l_run, alpha);
-      // O rescale when this row's reference max moved (warp-uniform TMEM access)
+        softmax_tile<64>(tS, lim0, lim1, kps, a.scale_log2, m_run, l_exact, l_round, alpha);
+      // O rescale when this row's reference max moved.  No further wait is needed: the
+      // MMA that produced this S tile was issued after this warpgroup's previous PV, and
+      // tcgen05 MMAs complete in issue order.  TMEM access is warp-collective, hence the
+      // vote.
       if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-        if (!wait_bar(&ctl->pv_done, (gg - 1) & 1, ctl, a.status, 22)) { ok = false; break; }
-        tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
-          tmem_ld_32x32b_x32(tO + c * 32, o);
+          tmem_ld_32x32b_x32(tOw + c * 32, o);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-          tmem_st_32x32b_x32(tO + c * 32, o);
+          tmem_st_32x32b_x32(tOw + c * 32, o);
         }
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->p_full[gg & 1]);
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->p_full[w]);
     }
     if (!ok) break;
-    g += n_tiles;
-    stat_m[buf * 128 + row] = m_run;
-    stat_l[buf * 128 + row] = l_run;
+    // ---- merge the two halves of the key walk, then this warpgroup's half of the output
+    float* st = stats + buf * (2 * 3 * 128);
+    st[(w * 3 + 0) * 128 + row] = m_run;
+    st[(w * 3 + 1) * 128 + row] = l_exact;
+    st[(w * 3 + 2) * 128 + row] = l_round;
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) {
-      mbar_arrive(&ctl->stats_full[buf]);
-      mbar_arrive(&ctl->list_empty[buf]);
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->stats_bar[buf]);
+    if (n_tiles > 0) {
+      if (!wait_bar(&ctl->o_full, ne_items & 1, ctl, a.status, 22)) break;
+      tc_fence_after();
     }
-  }
-}
-
-// ------------------------------------------------------------------------------------
-// epilogue warpgroup (warps 4-7)
-// ------------------------------------------------------------------------------------
-template <int BLOCK, bool JENGA>
-__device__ void epilogue_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t tmem,
-                              const CUtensorMap* to) {
-  using C = Cfg<BLOCK, JENGA>;
-  const int row = threadIdx.x - 128;       // 0..127
-  const uint32_t warp = threadIdx.x >> 5;  // 4..7
-  const uint32_t lane_base = ((warp & 3) * 32) << 16;
-  const float* stat_m = reinterpret_cast<const float*>(smem + kOffStats);
-  const float* stat_l = stat_m + 2 * 128;
-  const bool leader = threadIdx.x == 128;
-  for (uint32_t it = 0;; ++it) {
-    const uint32_t buf = it & 1;
-    if (!wait_bar(&ctl->list_full[buf], (it >> 1) & 1, ctl, a.status, 30)) break;
-    const int item = ctl->hdr_item[buf];
-    const int count = ctl->hdr_n[buf];
-    if (item < 0) break;
+    if (!wait_bar(&ctl->stats_bar[buf], (it >> 1) & 1, ctl, a.status, 23)) break;
+    float m[2], le[2], lr[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      m[h] = st[(h * 3 + 0) * 128 + row];
+      le[h] = st[(h * 3 + 1) * 128 + row];
+      lr[h] = st[(h * 3 + 2) * 128 + row];
+    }
+    const float mm = fmaxf(m[0], m[1]);
+    float c[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) c[h] = lr[h] > 0.0f ? fast_exp2(m[h] - mm) : 0.0f;
+    const float l_r = c[0] * lr[0] + c[1] * lr[1];
+    const float l_e = c[0] * le[0] + c[1] * le[1];
+    const bool has = l_r > 0.0f;
+    const float inv = has ? 1.0f / l_r : 0.0f;
+    const float f0 = c[0] * inv, f1 = c[1] * inv;
+    // a half's O is read only if that half attended something in this item (the other
+    // accumulator may still hold an earlier item's values)
+    const bool use0 = __any_sync(0xffffffffu, lr[0] > 0.0f);
+    const bool use1 = __any_sync(0xffffffffu, lr[1] > 0.0f);
     const int items_per_bh = a.nb / C::kPairs;
     const int bh = item / items_per_bh;
     const int qa = (item - bh * items_per_bh) * C::kPairs;
     const int row0 = bh * a.S + qa * BLOCK;
-    if (!wait_bar(&ctl->stats_full[buf], (it >> 1) & 1, ctl, a.status, 31)) break;
-    if (!wait_bar(&ctl->o_full[buf], (it >> 1) & 1, ctl, a.status, 32)) break;
-    tc_fence_after();
-    const float m = stat_m[buf * 128 + row];
-    const float l = stat_l[buf * 128 + row];
-    const bool has = l > 0.0f;
-    const float inv = has ? 1.0f / l : 0.0f;
-    uint8_t* qs = smem + kOffQ + buf * kQBytes;
-    const uint32_t tO = tmem + kColO + buf * 128 + lane_base;
+    uint8_t* qs = smem + kOffQ + buf * kTileBytes + w * (kTileBytes / 2);
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      uint32_t o[32];
-      if (count > 0) {
-        tmem_ld_32x32b_x32(tO + c * 32, o);
-        tmem_wait_ld();
-      }
+    for (int cc = 0; cc < 4; ++cc) {  // this warpgroup's 64 output columns, 16 at a time
+      const uint32_t col = w * 64 + cc * 16;
+      uint32_t o0[16], o1[16];
+      if (use0) tmem_ld_32x32b_x16(tO0 + col, o0);
+      if (use1) tmem_ld_32x32b_x16(tO1 + col, o1);
+      tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t w[4];
+      for (int i = 0; i < 2; ++i) {
+        uint32_t wv[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          float x0 = 0.0f, x1 = 0.0f;
-          if (has) {
-            x0 = __uint_as_float(o[8 * i + 2 * j]) * inv;
-            x1 = __uint_as_float(o[8 * i + 2 * j + 1]) * inv;
+          float x[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int k = 8 * i + 2 * j + u;
+            float v = 0.0f;
+            if (use0 && f0 != 0.0f) v = __uint_as_float(o0[k]) * f0;
+            if (use1 && f1 != 0.0f) v = fmaf(__uint_as_float(o1[k]), f1, v);
+            x[u] = v;
           }
-          w[j] = pack_bf16x2(x0, x1);
+          wv[j] = pack_bf16x2(x[0], x[1]);
         }
-        const uint32_t chunk = (uint32_t)((c & 1) * 4 + i);     // 16-byte chunk in the 128B row
-        const uint32_t phys = chunk ^ (uint32_t)(row & 7);      // 128-byte swizzle
-        uint8_t* dst = qs + (c >> 1) * (kQBytes / 2) + row * 128 + phys * 16;
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_addr(dst)), "r"(w[0]),
-                     "r"(w[1]), "r"(w[2]), "r"(w[3])
+        const uint32_t chunk = (uint32_t)(cc * 2 + i);      // 16-byte chunk in the 128B row
+        const uint32_t phys = chunk ^ (uint32_t)(row & 7);  // 128-byte swizzle
+        uint8_t* dst = qs + row * 128 + phys * 16;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_addr(dst)), "r"(wv[0]),
+                     "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
                      : "memory");
       }
     }
-    if (a.lse != nullptr) a.lse[(long long)row0 + row] = has ? m + log2f(l) : -3.402823466e+38f;
+    if (w == 0 && a.lse != nullptr)
+      a.lse[(long long)row0 + row] = has ? mm + log2f(l_e) : -3.402823466e+38f;
     tc_fence_before();
     fence_proxy_async_smem();
     __syncwarp();
     if ((threadIdx.x & 31) == 0) {
-      // O, the row statistics and the list header of this buffer are no longer needed
-      mbar_arrive(&ctl->o_empty[buf]);
+      if (n_tiles > 0) mbar_arrive(&ctl->o_empty);
       mbar_arrive(&ctl->list_empty[buf]);
-      mbar_arrive(&ctl->epi_bar[buf]);
+      mbar_arrive(&ctl->epi_bar[w]);
     }
+    if (n_tiles > 0) ++ne_items;
     if (leader) {
-      if (!wait_bar(&ctl->epi_bar[buf], (it >> 1) & 1, ctl, a.status, 33)) break;
-      tma_store_2d(to, qs, 0, row0);
-      tma_store_2d(to, qs + kQBytes / 2, 64, row0);
+      if (!wait_bar(&ctl->epi_bar[w], it & 1, ctl, a.status, 24)) break;
+      tma_store_2d(to, qs, w * 64, row0);
       bulk_commit_group();
       bulk_wait_group_read0();
       mbar_arrive(&ctl->q_empty[buf]);
@@ -570,28 +598,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&ctl->q_full[i], 1);
-      mbar_init(&ctl->q_empty[i], 1);
       mbar_init(&ctl->list_full[i], 1);
-      mbar_init(&ctl->list_empty[i], 9);
+      mbar_init(&ctl->list_empty[i], 9);  // the MMA thread + 8 softmax warps
+      mbar_init(&ctl->q_full[i], 1);
+      mbar_init(&ctl->q_empty[i], 2);     // one TMA-store leader per softmax warpgroup
       mbar_init(&ctl->s_full[i], 1);
       mbar_init(&ctl->p_full[i], 4);
-      mbar_init(&ctl->o_full[i], 1);
-      mbar_init(&ctl->o_empty[i], 4);
-      mbar_init(&ctl->stats_full[i], 4);
+      mbar_init(&ctl->stats_bar[i], 8);
       mbar_init(&ctl->epi_bar[i], 4);
     }
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&ctl->kv_full[i], 1);
       mbar_init(&ctl->kv_empty[i], 1);
     }
-    mbar_init(&ctl->pv_done, 1);
+    mbar_init(&ctl->o_full, 1);
+    mbar_init(&ctl->o_empty, 8);
     mbar_init(&ctl->drain, 1);
     ctl->abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 8) {
-    // the per-half byte maps start (and are always left) all zero
+    // the byte maps start (and are always left) all zero
     uint32_t* bm = reinterpret_cast<uint32_t*>(smem + kOffBm);
     for (int i = lane_id(); i < 2 * kMaxNb / 4; i += 32) bm[i] = 0;
     if (lane_id() == 0) {
@@ -610,15 +637,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
-  if (warp < 4) {
-    softmax_role<BLOCK, JENGA>(smem, ctl, a, tmem);
-  } else if (warp < 8) {
-    epilogue_role<BLOCK, JENGA>(smem, ctl, a, tmem, &to);
-  } else if (warp == 8) {
-    producer_role<BLOCK, JENGA>(smem, ctl, a, &tq, &tk, &tv);
+  if (warp < 8) {
+    regs_increase<kSoftmaxRegs>();
+    softmax_role<BLOCK, JENGA>(smem, ctl, a, tmem, (int)(warp >> 2), &to);
   } else {
-    if (lane_id() == 0) mma_role<BLOCK, JENGA>(smem, ctl, a, tmem);
-    __syncwarp();
+    regs_decrease<kOtherRegs>();
+    if (warp == 8) {
+      producer_role<BLOCK, JENGA>(smem, ctl, a, &tq, &tk, &tv);
+    } else if (warp == 9) {
+      if (lane_id() == 0) mma_role<BLOCK, JENGA>(smem, ctl, a, tmem);
+      __syncwarp();
+    }
   }
 
   tc_fence_before();
