@@ -284,6 +284,14 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
 __device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
   return f32x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
+// acc_lo += bf16 value in bits 0..15 of w, acc_hi += bf16 value in bits 16..31 (fp32 adds of
+// the exact bf16 values, no unpacking)
+__device__ __forceinline__ void add_bf16x2_to_f32(uint32_t w, float& acc_lo, float& acc_hi) {
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n add.rn.f32.bf16 %0, lo, %0;\n"
+      " add.rn.f32.bf16 %1, hi, %1;\n}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "r"(w));
+}
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

@@ -23,19 +23,21 @@
 //               never cause a duplicate or an out-of-bounds copy -- then TMA-loads Q
 //               (double-buffered across items) and ONLY the selected K/V blocks into a
 //               4-stage ring, in the order the MMA warp consumes them.
-//   warp 9      MMA issuer (one thread): S_t = Q K_t^T into TMEM S buffer t%2, then
-//               O_{t%2} += P_t V_t with P_t read from TMEM.  Issue order per item:
-//               QK0, QK1, PV0, QK2, PV1, ..., so QK_{t+1} runs while P_t is computed.
-//   warps 0-3   softmax warpgroup 0: the item's even key tiles;
-//   warps 4-7   softmax warpgroup 1: the item's odd key tiles.  One thread per query
-//               row; each warpgroup keeps its own running max m (log2 domain, allowed to
-//               lag the true max by up to 2^8 before O and l are rescaled), row sums and
-//               O accumulator, so the two never synchronise inside the key loop.
-//               After the item they merge (m, l, O) of both halves and each warpgroup
-//               normalises, stages and TMA-stores one 64-column half of the output;
-//               warpgroup 0 writes lse.
+//   warp 9      MMA issuer (one thread): S_g = Q K_g^T into TMEM S buffer g%2 (g counts
+//               key tiles across items), then, per key half w, O_w += P_g[:, 64w:64w+64]
+//               V_g[64w:64w+64, :] with P read from TMEM.  Issue order QK0, QK1, PV0,
+//               QK2, PV1, ..., so QK_{t+1} runs while P_t is computed.
+//   warps 0-3   softmax warpgroup 0: keys 0-63 of every key tile;
+//   warps 4-7   softmax warpgroup 1: keys 64-127 of every key tile.  One thread per
+//               query row; each warpgroup keeps its own running max m (log2 domain,
+//               allowed to lag the true max by up to 2^8 before O and l are rescaled),
+//               row sums and O accumulator, so the two never synchronise inside the key
+//               loop.  After the item they merge (m, l, O) of both halves and each
+//               warpgroup normalises, stages and TMA-stores one 64-column half of the
+//               output; warpgroup 0 writes lse.
 //   warps 10-11 idle.
-// TMEM (512 columns): S0, S1 at columns 0, 128; O0, O1 at 256, 384.
+// TMEM (512 columns): S0, S1 at columns 0, 128 (warpgroup w reads S columns 64w..64w+63
+// and writes its bf16 P over the first 32 of them); O0, O1 at 256, 384.
 // Every mbarrier wait is bounded; a wait that runs out records a code in the device
 // status word, raises the CTA's abort flag and every role returns.
 #pragma once
@@ -79,7 +81,11 @@ struct SmemCtl {
   uint64_t list_full[2], list_empty[2];
   uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2], p_full[2];
+  uint64_t s_full[2];   // S buffer b holds a fresh tile
+  uint64_t p_full[2][2];  // [w][b]: warpgroup w has written its P half of S buffer b
+                          // (per buffer, so a warp running a tile ahead of its siblings
+                          // can never complete the previous tile's phase)
+  uint64_t pv_done[2];  // warpgroup w's PV half has completed
   uint64_t o_full, o_empty;
   uint64_t stats_bar[2];
   uint64_t epi_bar[2];
@@ -287,7 +293,9 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
   constexpr uint32_t kIdescS64 = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);
   uint32_t L = 0;            // ring position
-  uint32_t gt[2] = {0, 0};   // tiles issued per softmax warpgroup (S buffer / P phases)
+  uint32_t g = 0;            // key tiles issued so far, across items (S buffer g & 1)
+  uint32_t gw[2] = {0, 0};   // PV halves issued per warpgroup (PV-done phases)
+  uint32_t pc[2][2] = {{0, 0}, {0, 0}};  // P phases per (warpgroup, S buffer)
   uint32_t ne_items = 0;     // non-empty items so far (O phases)
   uint32_t nq[2] = {0, 0};   // Q fills consumed per Q buffer
   for (uint32_t it = 0;; ++it) {
@@ -303,10 +311,10 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
     ++nq[buf];
     tc_fence_after();
     const uint32_t qaddr = smem_addr(smem + kOffQ + buf * kTileBytes);
+    bool first[2] = {true, true};  // next PV half w is the item's first into O_w
     bool ok = true;
     for (int t = 0; t <= n_tiles && ok; ++t) {
-      if (t < n_tiles) {  // S_t = Q K_t^T into S buffer t%2
-        const int w = t & 1;
+      if (t < n_tiles) {  // S = Q K_t^T into S buffer (g + t) & 1
         const uint32_t stage = L % kStages;
         if (!wait_bar(&ctl->kv_full[stage], (L / kStages) & 1, ctl, a.status, 12)) {
           ok = false;
@@ -316,7 +324,8 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
         const int ne = (count - t * C::kSub) < C::kSub ? (count - t * C::kSub) : C::kSub;
         const uint32_t idesc = (ne * BLOCK == 128) ? kIdescS128 : kIdescS64;
         const uint32_t kaddr = smem_addr(smem + kOffKV + stage * kTileBytes);
-        const uint32_t tS = tmem + kColS + w * 128;
+        const uint32_t sb = (g + t) & 1;
+        const uint32_t tS = tmem + kColS + sb * 128;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = (k >> 2) * (kTileBytes / 2) + (k & 3) * 32;
@@ -324,18 +333,13 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
                  idesc, k > 0);
         }
         mma_commit(&ctl->kv_empty[stage]);
-        mma_commit(&ctl->s_full[w]);
+        mma_commit(&ctl->s_full[sb]);
         ++L;
       }
-      if (t >= 1) {  // O_{w} += P_{t-1} V_{t-1}
+      if (t >= 1) {  // O_w += P V for the previous tile, one key half per warpgroup
         const int tp = t - 1;
-        const int w = tp & 1;
         if (tp == 0 && ne_items >= 1 &&
             !wait_bar(&ctl->o_empty, (ne_items - 1) & 1, ctl, a.status, 13)) {
-          ok = false;
-          break;
-        }
-        if (!wait_bar(&ctl->p_full[w], gt[w] & 1, ctl, a.status, 14)) {
           ok = false;
           break;
         }
@@ -344,22 +348,38 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
           ok = false;
           break;
         }
-        tc_fence_after();
         const int ne = (count - tp * C::kSub) < C::kSub ? (count - tp * C::kSub) : C::kSub;
-        const int ksteps = ne * BLOCK / 16;
+        const int halves = (ne * BLOCK) / 64;  // 1 for a 64-key tile, else 2
         const uint32_t vaddr = smem_addr(smem + kOffKV + stage * kTileBytes);
-        const uint32_t tP = tmem + kColS + w * 128;
-        const uint32_t tO = tmem + kColO + w * 128;
-        for (int k = 0; k < ksteps; ++k) {
-          mma_ts(tO, tP + k * 8, smem_desc_sw128(vaddr + k * 2048, kTileBytes / 2, 1024), kIdescPV,
-                 (tp >= 2 || k > 0) ? 1u : 0u);
+        const uint32_t pb = (g + tp) & 1;
+        const uint32_t tS = tmem + kColS + pb * 128;
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          if (w >= halves) break;
+          if (!wait_bar(&ctl->p_full[w][pb], pc[w][pb] & 1, ctl, a.status, 14)) {
+            ok = false;
+            break;
+          }
+          ++pc[w][pb];
+          tc_fence_after();
+          const uint32_t tO = tmem + kColO + w * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            mma_ts(tO, tS + w * 64 + k * 8,
+                   smem_desc_sw128(vaddr + w * 8192 + k * 2048, kTileBytes / 2, 1024), kIdescPV,
+                   (!first[w] || k > 0) ? 1u : 0u);
+          }
+          mma_commit(&ctl->pv_done[w]);
+          first[w] = false;
+          ++gw[w];
         }
+        if (!ok) break;
         mma_commit(&ctl->kv_empty[stage]);
-        ++gt[w];
         ++L;
       }
     }
     if (!ok) break;
+    g += n_tiles;
     mma_commit(&ctl->o_full);
     ++ne_items;
   }
@@ -412,7 +432,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, int lim0, int lim1, in
   const float neg = (m_run == -INFINITY) ? 0.0f : -m_run;
   const uint64_t sl2x2 = f32x2(sl2, sl2), negx2 = f32x2(neg, neg);
   uint64_t acc_e[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
-  uint64_t acc_r[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+  float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
   uint32_t pk[NK / 2];
 #pragma unroll
   for (int i = 0; i < NK / 2; ++i) {
@@ -421,13 +441,14 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, int lim0, int lim1, in
     const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
     acc_e[i & 1] = add_f32x2(acc_e[i & 1], f32x2(p0, p1));
     pk[i] = pack_bf16x2(p0, p1);
-    acc_r[i & 1] = add_f32x2(acc_r[i & 1], bf16x2_to_f32x2(pk[i]));
+    if (i & 1)
+      add_bf16x2_to_f32(pk[i], r2, r3);
+    else
+      add_bf16x2_to_f32(pk[i], r0, r1);
   }
-  float e0, e1, e2, e3, r0, r1, r2, r3;
+  float e0, e1, e2, e3;
   split_f32x2(acc_e[0], e0, e1);
   split_f32x2(acc_e[1], e2, e3);
-  split_f32x2(acc_r[0], r0, r1);
-  split_f32x2(acc_r[1], r2, r3);
   l_exact = l_exact * alpha + ((e0 + e1) + (e2 + e3));
   l_round = l_round * alpha + ((r0 + r1) + (r2 + r3));
 #pragma unroll
@@ -439,16 +460,16 @@ template <int BLOCK, bool JENGA>
 __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t tmem,
                              int w, const CUtensorMap* to) {
   using C = Cfg<BLOCK>;
-  constexpr int kps = BLOCK;  // keys per key block
   const int row = threadIdx.x & 127;
   const uint32_t lane_base = (((threadIdx.x >> 5) & 3) * 32) << 16;  // warp's TMEM lanes
   const uint32_t half = (BLOCK == 64) ? (uint32_t)(row >> 6) : 0u;
-  const uint32_t tS = tmem + kColS + w * 128 + lane_base;
   const uint32_t tO0 = tmem + kColO + lane_base, tO1 = tO0 + 128;
   const uint32_t tOw = w ? tO1 : tO0;
   float* stats = reinterpret_cast<float*>(smem + kOffStats);  // [par][wg][3][128]
   const bool leader = row == 0;
-  uint32_t gw = 0, ne_items = 0;
+  uint32_t g = 0;         // key tiles seen so far, across items (S buffer g & 1)
+  uint32_t gw = 0;        // tiles this warpgroup took part in (P / PV phases)
+  uint32_t ne_items = 0;
   for (uint32_t it = 0;; ++it) {
     const uint32_t buf = it & 1;
     if (!wait_bar(&ctl->list_full[buf], (it >> 1) & 1, ctl, a.status, 20)) break;
@@ -459,26 +480,35 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
     const int n_tiles = (count + C::kSub - 1) / C::kSub;
     float m_run = -INFINITY, l_exact = 0.0f, l_round = 0.0f;
     bool ok = true;
-    for (int t = w; t < n_tiles; t += 2, ++gw) {
+    bool started = false;  // this warpgroup has a PV in flight for this item
+    for (int t = 0; t < n_tiles; ++t, ++g) {
       const int e0 = t * C::kSub;
       const int ne = (count - e0) < C::kSub ? (count - e0) : C::kSub;
-      const int lim0 = entry_limit(list[e0], half);
-      const int lim1 = ne > 1 ? entry_limit(list[e0 + 1], half) : kps;
-      if (!wait_bar(&ctl->s_full[w], gw & 1, ctl, a.status, 21)) {
+      if (ne * BLOCK / 64 <= w) continue;  // a 64-key tile has no second half
+      int lim;
+      if (BLOCK == 64) {
+        lim = entry_limit(list[e0 + w], half);
+      } else {
+        lim = entry_limit(list[e0], half) - 64 * w;
+        lim = lim < 0 ? 0 : (lim > 64 ? 64 : lim);
+      }
+      const uint32_t sb = g & 1;
+      if (!wait_bar(&ctl->s_full[sb], (g >> 1) & 1, ctl, a.status, 21)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      const uint32_t tS = tmem + kColS + sb * 128 + 64 * w + lane_base;
       float alpha;
-      if (ne * BLOCK == 128)
-        softmax_tile<128>(tS, lim0, lim1, kps, a.scale_log2, m_run, l_exact, l_round, alpha);
-      else
-        softmax_tile<64>(tS, lim0, lim1, kps, a.scale_log2, m_run, l_exact, l_round, alpha);
-      // O rescale when this row's reference max moved.  No further wait is needed: the
-      // MMA that produced this S tile was issued after this warpgroup's previous PV, and
-      // tcgen05 MMAs complete in issue order.  TMEM access is warp-collective, hence the
-      // vote.
-      if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+      softmax_tile<64>(tS, lim, 64, 64, a.scale_log2, m_run, l_exact, l_round, alpha);
+      // O rescale when this row's reference max moved: wait until this warpgroup's
+      // previous PV has completed (TMEM access is warp-collective, hence the vote).
+      if (__any_sync(0xffffffffu, alpha != 1.0f) && started) {
+        if (!wait_bar(&ctl->pv_done[w], (gw - 1) & 1, ctl, a.status, 25)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
@@ -492,7 +522,9 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->p_full[w]);
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->p_full[w][sb]);
+      ++gw;
+      started = true;
     }
     if (!ok) break;
     // ---- merge the two halves of the key walk, then this warpgroup's half of the output
@@ -603,7 +635,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->q_full[i], 1);
       mbar_init(&ctl->q_empty[i], 2);     // one TMA-store leader per softmax warpgroup
       mbar_init(&ctl->s_full[i], 1);
-      mbar_init(&ctl->p_full[i], 4);
+      mbar_init(&ctl->p_full[i][0], 4);
+      mbar_init(&ctl->p_full[i][1], 4);
+      mbar_init(&ctl->pv_done[i], 1);
       mbar_init(&ctl->stats_bar[i], 8);
       mbar_init(&ctl->epi_bar[i], 4);
     }
