@@ -129,6 +129,17 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, dist, device=None) -> float:
+    """Largest value of ``x`` over all ranks (x itself without a process group); the
+    tensor lives on ``device`` (CUDA for NCCL, CPU for gloo)."""
+    if dist is None or not dist.is_initialized():
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def oracle_sample(w, budget_s: float, seed: int = 0):
     """Time the oracle on whole query blocks, head-major order from a seeded shuffle,
     adding blocks until about ``budget_s`` seconds of CPU work; returns
@@ -295,11 +306,7 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = sum(times) / len(times)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(times) / len(times), dist, dev)
     code, detail = binding.vsa_device_status()
     if code != binding.VSA_OK:
         raise RuntimeError(f"device status {code} detail {detail:#x} after timing")
@@ -330,11 +337,7 @@ def main():
                                       w.block, w.scale, h_out, h_lse, bufs, workspace=wsbuf,
                                       stream=stream)
             stream.synchronize()
-        e2e_ms = (time.perf_counter() - t0) / args.e2e_steps * 1e3
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps * 1e3, dist, dev)
         e2e = {"value": ws * pairs * flop_per_pair / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
@@ -370,8 +373,9 @@ def main():
 
 
 # DRAM bytes (read + write) per launch of the forward kernel from an ncu capture of the
-# same kernel build, per workload; None until measured for the current kernel.
-TRAFFIC = {}
+# same kernel build (profiles/bsa_fwd_kernel_<workload>.md); absent = not measured for
+# the current kernel.
+TRAFFIC = {"vsa_mid": 182.4e6, "vsa_blk128": 1602.6e6}
 
 
 if __name__ == "__main__":
