@@ -28,7 +28,7 @@ MAX_BLOCKS = 2048
 # every symbol include/vsa.h declares
 EXPORTS = ("vsa_fwd", "jenga_fwd", "vsa_workspace_bytes", "vsa_lut_to_bitmap",
            "vsa_bitmap_to_lut", "vsa_fwd_from_host", "vsa_device_status",
-           "vsa_last_launch_count", "vsa_status_str")
+           "vsa_last_launch_count", "vsa_status_str", "vsa_fwd_noalloc")
 
 
 class VsaError(RuntimeError):
@@ -56,6 +56,8 @@ def load(path: str = LIB_PATH):
     h.vsa_fwd.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P, P, P]
     h.jenga_fwd.restype = i32
     h.jenga_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P, P, P]
+    h.vsa_fwd_noalloc.restype = i32
+    h.vsa_fwd_noalloc.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P, P]
     h.vsa_workspace_bytes.restype = sz
     h.vsa_workspace_bytes.argtypes = []
     h.vsa_lut_to_bitmap.restype = i32
@@ -158,6 +160,32 @@ def vsa_fwd(q, k, v, q2k_idx, q2k_num, variable_block_sizes, block=None, scale=N
                      _stream(stream))
     _check("vsa_fwd", code)
     return out, lse_t
+
+
+def vsa_fwd_noalloc(q, k, v, q2k_idx, q2k_num, variable_block_sizes, block=None, scale=None,
+                    out=None, lse=None, stream=None):
+    """vsa_fwd for callers that cannot hand the library any device memory of their own:
+    the scheduling scratch lives in a static array inside the library (shared by every
+    call on the device, so calls must not overlap on the GPU).  ``out`` and ``lse`` must
+    be given when the caller cannot allocate (they are allocated here only if omitted).
+    Returns (out, lse or None)."""
+    h = load()
+    _dev(q, "q", torch.bfloat16, 4)
+    B, H, S, D = q.shape
+    vbs = _meta32(variable_block_sizes, "variable_block_sizes")
+    nb = vbs.numel()
+    if block is None:
+        block = S // nb if nb and S % nb == 0 else 0
+    idx = _meta32(q2k_idx, "q2k_idx")
+    num = _meta32(q2k_num, "q2k_num")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    code = h.vsa_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(num), _ptr(vbs), B, H,
+                             S, D, idx.shape[-1], block, scale, _ptr(out), _ptr(lse),
+                             _stream(stream))
+    _check("vsa_fwd_noalloc", code)
+    return out, lse
 
 
 def jenga_fwd(q, k, v, mask_bitmap, block_q=64, block_k=64, scale=None, out=None, lse=True,

@@ -355,6 +355,73 @@ vsa_status vsa_device_status(vsa_stream_t stream, unsigned int* detail) {
 
 int vsa_last_launch_count(void) { return t_last_launches; }
 
+}  // extern "C"
+
+// ------------------------------------------------------------------ allocation-free entry
+// Scheduling scratch of vsa_fwd_noalloc: a file-scope device array used in place of the
+// caller-provided workspace of vsa_fwd.  Every GPU that loads this library holds these
+// VSA_NOALLOC_SCRATCH_BYTES bytes until the process exits; all calls on a device share
+// them.
+static __device__ __align__(256) unsigned int g_noalloc_scratch[VSA_NOALLOC_SCRATCH_BYTES / 4];
+
+namespace {
+void* g_noalloc_addr[64] = {};  // device address of g_noalloc_scratch, per device
+
+// Argument checks of vsa_fwd, repeated here so that nothing is enqueued (not even the
+// scratch reset) for a call that vsa_fwd would reject.
+vsa_status noalloc_checks(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
+                          const int32_t* q2k_idx, const int32_t* q2k_num,
+                          const int32_t* vbs, int B, int H, int S, int D, int max_kv,
+                          int block, float scale, const vsa_bf16* out, const float* lse,
+                          bool* nothing) {
+  DeviceInfo* dev = nullptr;
+  vsa_status st = common_checks(q, k, v, out, B, H, S, D, block, scale, &dev, nothing);
+  if (st != VSA_OK || *nothing) return st;
+  if (max_kv < 1) return VSA_ERR_INVALID_ARG;
+  if (!q2k_idx || !q2k_num || !vbs) return VSA_ERR_INVALID_ARG;
+  if (lse && overlaps(lse, (size_t)B * H * S * 4, out, (size_t)B * H * S * D * 2))
+    return VSA_ERR_INVALID_ARG;
+  return VSA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+vsa_status vsa_fwd_noalloc(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
+                           const int32_t* q2k_idx, const int32_t* q2k_num,
+                           const int32_t* variable_block_sizes, int B, int H, int S, int D,
+                           int max_kv, int block, float scale, vsa_bf16* out, float* lse,
+                           vsa_stream_t stream) {
+  t_last_launches = 0;
+  // the scratch this call needs must fit the static array
+  if (vsa_workspace_bytes() > (size_t)VSA_NOALLOC_SCRATCH_BYTES) return VSA_ERR_UNSUPPORTED;
+  bool nothing = false;
+  vsa_status st = noalloc_checks(q, k, v, q2k_idx, q2k_num, variable_block_sizes, B, H, S, D,
+                                 max_kv, block, scale, out, lse, &nothing);
+  if (st != VSA_OK || nothing) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return VSA_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    // set-up, once per device, with that device current: the array's device address
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+        return VSA_ERR_CUDA;
+      g_noalloc_addr[dev] = p;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  // the array keeps whatever the previous call left: the scheduling counters must start
+  // at zero, so clear them in stream order before the kernel
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(scratch, 0, vsa_workspace_bytes(), s) != cudaSuccess) return VSA_ERR_CUDA;
+  st = vsa_fwd(q, k, v, q2k_idx, q2k_num, variable_block_sizes, B, H, S, D, max_kv, block,
+               scale, out, lse, scratch, stream);
+  return st;
+}
+
 const char* vsa_status_str(vsa_status s) {
   switch (s) {
     case VSA_OK: return "ok";

@@ -118,6 +118,33 @@ VSA_API vsa_status jenga_fwd(const vsa_bf16 *q, const vsa_bf16 *k, const vsa_bf1
 /* Bytes of device workspace vsa_fwd / jenga_fwd use when given one. */
 VSA_API size_t vsa_workspace_bytes(void);
 
+/* Size of the library's own scheduling scratch used by vsa_fwd_noalloc. */
+#define VSA_NOALLOC_SCRATCH_BYTES 256
+
+/* vsa_fwd for callers that cannot allocate device memory.  (The pages describe no such
+ * entry point; it exists for this library's users.)  Some callers have no way to obtain
+ * a workspace buffer: a plug-in whose host framework owns every device allocation and
+ * offers no hook for extra buffers, or a serving loop that must not call cudaMalloc once
+ * it is running because cudaMalloc can synchronise the device and stall other streams.
+ * This entry point takes the same arguments as vsa_fwd minus `workspace`, allocates
+ * nothing and calls no allocating routine: its dynamic-schedule scratch is a static
+ * device array of VSA_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU
+ * that loads the library keeps until the process exits.
+ *   - The first call on a device looks up that array's device address (with the device
+ *     current) and caches it; make that first call before any stream capture begins.
+ *   - Every call on a device shares the array.  Each call clears the scheduling counters
+ *     in stream order before its kernel, so calls on one stream are safe; calls that
+ *     overlap on the GPU (different streams without ordering between them) race on the
+ *     counters and must not be issued.
+ *   - A call whose scratch need exceeds VSA_NOALLOC_SCRATCH_BYTES returns
+ *     VSA_ERR_UNSUPPORTED; other errors are those of vsa_fwd, checked before anything
+ *     is enqueued. */
+VSA_API vsa_status vsa_fwd_noalloc(const vsa_bf16 *q, const vsa_bf16 *k, const vsa_bf16 *v,
+                                   const int32_t *q2k_idx, const int32_t *q2k_num,
+                                   const int32_t *variable_block_sizes, int B, int H, int S,
+                                   int D, int max_kv, int block, float scale, vsa_bf16 *out,
+                                   float *lse, vsa_stream_t stream);
+
 /* LUT -> bitmap, bit-exact: bitmap[r, kb] = 1 iff kb is one of the first
  * clamp(q2k_num[r], 0, max_kv) entries of q2k_idx row r (entries outside [0, nb)
  * skipped), else 0.  q2k_idx [rows, max_kv], q2k_num [rows], bitmap [rows, nb] int8.
