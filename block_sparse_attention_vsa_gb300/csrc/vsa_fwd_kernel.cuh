@@ -499,8 +499,18 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
       }
       tc_fence_after();
       const uint32_t tS = tmem + kColS + sb * 128 + 64 * w + lane_base;
-      float alpha;
-      softmax_tile<64>(tS, lim, 64, 64, a.scale_log2, m_run, l_exact, l_round, alpha);
+      float alpha = 1.0f;
+      if (lim > 0) {
+        softmax_tile<64>(tS, lim, 64, 64, a.scale_log2, m_run, l_exact, l_round, alpha);
+      } else {
+        // none of this warp's rows attends these keys (a block selected only by the other
+        // query block of the pair, or a zero-width tail): P = 0, the running state stays.
+        // lim depends only on the row's query half, so the branch is warp-uniform.
+        uint32_t z[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = 0u;
+        tmem_st_32x32b_x32(tS, z);
+      }
       // O rescale when this row's reference max moved: wait until this warpgroup's
       // previous PV has completed (TMEM access is warp-collective, hence the vote).
       if (__any_sync(0xffffffffu, alpha != 1.0f) && started) {
