@@ -310,7 +310,7 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
     if (!wait_bar(&ctl->q_full[buf], nq[buf] & 1, ctl, a.status, 11)) break;
     ++nq[buf];
     tc_fence_after();
-    const uint32_t qaddr = smem_addr(smem + kOffQ + buf * kTileBytes);
+    const uint64_t qdesc = smem_desc_sw128(smem_addr(smem + kOffQ + buf * kTileBytes), 16, 1024);
     bool first[2] = {true, true};  // next PV half w is the item's first into O_w
     bool ok = true;
     for (int t = 0; t <= n_tiles && ok; ++t) {
@@ -323,14 +323,15 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
         tc_fence_after();
         const int ne = (count - t * C::kSub) < C::kSub ? (count - t * C::kSub) : C::kSub;
         const uint32_t idesc = (ne * BLOCK == 128) ? kIdescS128 : kIdescS64;
-        const uint32_t kaddr = smem_addr(smem + kOffKV + stage * kTileBytes);
+        const uint64_t kdesc =
+            smem_desc_sw128(smem_addr(smem + kOffKV + stage * kTileBytes), 16, 1024);
         const uint32_t sb = (g + t) & 1;
         const uint32_t tS = tmem + kColS + sb * 128;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * (kTileBytes / 2) + (k & 3) * 32;
-          mma_ss(tS, smem_desc_sw128(qaddr + off, 16, 1024), smem_desc_sw128(kaddr + off, 16, 1024),
-                 idesc, k > 0);
+          // the descriptor's start address is addr >> 4 in its low bits: step by offset >> 4
+          const uint64_t off16 = ((k >> 2) * (kTileBytes / 2) + (k & 3) * 32) >> 4;
+          mma_ss(tS, qdesc + off16, kdesc + off16, idesc, k > 0);
         }
         mma_commit(&ctl->kv_empty[stage]);
         mma_commit(&ctl->s_full[sb]);
@@ -350,7 +351,8 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
         }
         const int ne = (count - tp * C::kSub) < C::kSub ? (count - tp * C::kSub) : C::kSub;
         const int halves = (ne * BLOCK) / 64;  // 1 for a 64-key tile, else 2
-        const uint32_t vaddr = smem_addr(smem + kOffKV + stage * kTileBytes);
+        const uint64_t vdesc =
+            smem_desc_sw128(smem_addr(smem + kOffKV + stage * kTileBytes), kTileBytes / 2, 1024);
         const uint32_t pb = (g + tp) & 1;
         const uint32_t tS = tmem + kColS + pb * 128;
 #pragma unroll
@@ -365,8 +367,7 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
           const uint32_t tO = tmem + kColO + w * 128;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            mma_ts(tO, tS + w * 64 + k * 8,
-                   smem_desc_sw128(vaddr + w * 8192 + k * 2048, kTileBytes / 2, 1024), kIdescPV,
+            mma_ts(tO, tS + w * 64 + k * 8, vdesc + ((w * 8192 + k * 2048) >> 4), kIdescPV,
                    (!first[w] || k > 0) ? 1u : 0u);
           }
           mma_commit(&ctl->pv_done[w]);
