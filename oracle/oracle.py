@@ -73,8 +73,8 @@ def load(lib: str = LIB, src: str = SRC):
     h.oracle_blockmask_to_lut.restype = None
     h.oracle_blockmask_to_lut.argtypes = [P, i64, i32, i32, P, P]
     h.oracle_masked_attention.restype = None
-    h.oracle_masked_attention.argtypes = [P, P, P, i32, i32, i32, i32, P, i64, i64,
-                                          i32, i32, P, f64, P, i64, P, P]
+    h.oracle_masked_attention.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P, i64,
+                                          i64, i32, P, f64, P, i64, P, P]
     if lib == LIB:
         _lib = h
     return h
@@ -125,9 +125,11 @@ def all_qblocks(B: int, H: int, nb: int) -> np.ndarray:
 
 def masked_attention(q_bits, k_bits, v_bits, blockmask, block: int, scale: float,
                      vbs=None, sel=None, h=None):
-    """Oracle forward on bf16 bit patterns (uint16 [B,H,S,D]).
+    """Oracle forward on bf16 bit patterns: q uint16 [B,Hq,Sq,D], k and v [B,Hkv,Sk,D]
+    (Hq a multiple of Hkv; query head h reads key/value head h // (Hq // Hkv)).
 
-    blockmask: int8 [B,H,nb,nb] (per head) or [nb,nb] (shared by all B,H).
+    blockmask: int8 [B,Hq,nbq,nbk] (per head) or [nbq,nbk] (shared by all B,H),
+    nbq = Sq // block, nbk = Sk // block.  vbs: int32 [nbk] or None (full blocks).
     sel: int32 [n,3] of (b,h,qb); default every q-block.
     Returns (out float64 [n,block,D], lse float64 [n,block]).
     """
@@ -135,37 +137,38 @@ def masked_attention(q_bits, k_bits, v_bits, blockmask, block: int, scale: float
     q = _c(q_bits, np.uint16)
     k = _c(k_bits, np.uint16)
     v = _c(v_bits, np.uint16)
-    B, H, S, D = q.shape
-    assert k.shape == q.shape and v.shape == q.shape
-    assert S % block == 0
-    nb = S // block
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    assert v.shape == k.shape and Bk == B and Dk == D and Hq % Hkv == 0
+    assert Sq % block == 0 and Sk % block == 0
+    nbq, nbk = Sq // block, Sk // block
     m = _c(blockmask, np.int8)
     if m.ndim == 2:
-        assert m.shape == (nb, nb)
+        assert m.shape == (nbq, nbk)
         sb, sh = 0, 0
     else:
-        assert m.shape == (B, H, nb, nb)
-        sb, sh = H, 1
+        assert m.shape == (B, Hq, nbq, nbk)
+        sb, sh = Hq, 1
     vb = None if vbs is None else _c(vbs, np.int32)
     if vb is not None:
-        assert vb.shape == (nb,)
-    s = all_qblocks(B, H, nb) if sel is None else _c(sel, np.int32).reshape(-1, 3)
+        assert vb.shape == (nbk,)
+    s = all_qblocks(B, Hq, nbq) if sel is None else _c(sel, np.int32).reshape(-1, 3)
     n = s.shape[0]
     out = np.empty((n, block, D), dtype=np.float64)
     lse = np.empty((n, block), dtype=np.float64)
-    h.oracle_masked_attention(_ptr(q), _ptr(k), _ptr(v), B, H, S, D, _ptr(m), sb, sh, nb,
-                              block, None if vb is None else _ptr(vb), float(scale),
+    h.oracle_masked_attention(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Sk, D, _ptr(m), sb,
+                              sh, block, None if vb is None else _ptr(vb), float(scale),
                               _ptr(s), n, _ptr(out), _ptr(lse))
     return out, lse
 
 
 def vsa_forward(q_bits, k_bits, v_bits, q2k_idx, q2k_num, vbs, block: int, scale: float,
                 sel=None, h=None):
-    """VSA forward: LUT [B,H,nb,max_kv] + counts [B,H,nb] -> block mask -> masked attention."""
+    """VSA forward: LUT [B,Hq,nbq,max_kv] + counts [B,Hq,nbq] -> block mask -> masked
+    attention (key blocks nbk = Sk // block)."""
     h = h or load()
-    S = q_bits.shape[2]
-    nb = S // block
-    mask = lut_to_blockmask(q2k_idx, q2k_num, nb, h=h)
+    nbk = k_bits.shape[2] // block
+    mask = lut_to_blockmask(q2k_idx, q2k_num, nbk, h=h)
     return masked_attention(q_bits, k_bits, v_bits, mask, block, scale, vbs=vbs, sel=sel, h=h)
 
 

@@ -48,6 +48,12 @@
  *      count 0 produce exactly-zero output rows (and a finite LSE
  *      sentinel)"; the value -FLT_MAX is this library's reading).
  *
+ * Grouped-query and cross-length attention ("TheRock rocke sparse_attention.py",
+ * JengaSparseSpec / VsaSparseSpec: separate seqlen_q / seqlen_k and query / key-value
+ * head counts, kv_head_idx): q is [B, Hq, Sq, D], k and v are [B, Hkv, Sk, D] with Hq a
+ * multiple of Hkv; query head h reads key/value head h / (Hq / Hkv); query blocks are
+ * Sq / block, key blocks Sk / block, and the block mask is [Sq/block, Sk/block].
+ *
  * Metadata conversions (bit-exact references for the device converters):
  *   - LUT -> bitmap: step 1 above written as i8 0/1.
  *   - bitmap -> LUT: ascending compaction of the nonzero bytes of a row,
@@ -125,48 +131,53 @@ void oracle_blockmask_to_lut(const int8_t *mask, int64_t rows, int nb,
 
 /* Steps 2-4 for a list of query blocks.
  *
- *   q, k, v     bf16 bits, [B, H, S, D] contiguous.
- *   blockmask   int8 0/1 (any nonzero = attend), [*, nb, nb]: entry
- *               (b, h) starts at  b*mask_stride_b + h*mask_stride_h
- *               (strides in units of nb*nb; both 0 = one mask shared by
- *               every batch and head, as for the Jenga bitmap).
- *   vbs         int32 [nb] valid key counts per k-block, or NULL = block.
+ *   q           bf16 bits, [B, Hq, Sq, D] contiguous.
+ *   k, v        bf16 bits, [B, Hkv, Sk, D] contiguous; Hq a multiple of Hkv.
+ *   blockmask   int8 0/1 (any nonzero = attend), [*, nbq, nbk] with
+ *               nbq = Sq / block, nbk = Sk / block: entry (b, h) starts at
+ *               b*mask_stride_b + h*mask_stride_h (strides in units of
+ *               nbq*nbk; both 0 = one mask shared by every batch and head,
+ *               as for the Jenga bitmap).
+ *   vbs         int32 [nbk] valid key counts per k-block, or NULL = block.
  *   sel         int32 triples (b, h, qb), n_sel of them: the query blocks
  *               to compute.
  *   out         double [n_sel, block, D];  lse double [n_sel, block].
  */
 void oracle_masked_attention(const uint16_t *q, const uint16_t *k,
-                             const uint16_t *v, int B, int H, int S, int D,
-                             const int8_t *blockmask, int64_t mask_stride_b,
-                             int64_t mask_stride_h, int nb, int block,
-                             const int32_t *vbs, double scale,
+                             const uint16_t *v, int B, int Hq, int Hkv, int Sq,
+                             int Sk, int D, const int8_t *blockmask,
+                             int64_t mask_stride_b, int64_t mask_stride_h,
+                             int block, const int32_t *vbs, double scale,
                              const int32_t *sel, int64_t n_sel, double *out,
                              double *lse) {
   (void)B;
+  const int nbq = Sq / block, nbk = Sk / block;
+  const int group = Hq / Hkv;
 #pragma omp parallel
   {
-    double *s_buf = (double *)malloc(sizeof(double) * (size_t)S);
-    int32_t *j_buf = (int32_t *)malloc(sizeof(int32_t) * (size_t)S);
+    double *s_buf = (double *)malloc(sizeof(double) * (size_t)Sk);
+    int32_t *j_buf = (int32_t *)malloc(sizeof(int32_t) * (size_t)Sk);
     double *qrow = (double *)malloc(sizeof(double) * (size_t)D);
     double *acc = (double *)malloc(sizeof(double) * (size_t)D);
 #pragma omp for schedule(dynamic, 1)
     for (int64_t t = 0; t < n_sel; ++t) {
       const int b = sel[3 * t + 0], h = sel[3 * t + 1], qb = sel[3 * t + 2];
-      const int64_t bh = (int64_t)b * H + h;
-      const uint16_t *qh = q + bh * S * (int64_t)D;
-      const uint16_t *kh = k + bh * S * (int64_t)D;
-      const uint16_t *vh = v + bh * S * (int64_t)D;
+      const int64_t bh = (int64_t)b * Hq + h;
+      const int64_t bkv = (int64_t)b * Hkv + h / group;
+      const uint16_t *qh = q + bh * Sq * (int64_t)D;
+      const uint16_t *kh = k + bkv * Sk * (int64_t)D;
+      const uint16_t *vh = v + bkv * Sk * (int64_t)D;
       const int8_t *mrow = blockmask +
                            (b * mask_stride_b + h * mask_stride_h) *
-                               (int64_t)nb * nb +
-                           (int64_t)qb * nb;
+                               (int64_t)nbq * nbk +
+                           (int64_t)qb * nbk;
       for (int r = 0; r < block; ++r) {
         const int i = qb * block + r;
         double *orow = out + (t * block + r) * (int64_t)D;
         for (int d = 0; d < D; ++d) qrow[d] = bf16_to_double(qh[(int64_t)i * D + d]);
         /* pass 1: the attended set (token mask, ascending j) and its scores */
         int64_t n_att = 0;
-        for (int j = 0; j < S; ++j) {
+        for (int j = 0; j < Sk; ++j) {
           const int kb = j / block;
           const int valid = vbs ? vbs[kb] : block;
           if (mrow[kb] == 0 || (j % block) >= valid) continue;

@@ -35,6 +35,9 @@ MUTANTS = {
     "lut_descending": ("for (int kb = 0; kb < nb; ++kb) {\n      if (mrow[kb] != 0) {",
                        "for (int kb = nb - 1; kb >= 0; --kb) {\n      if (mrow[kb] != 0) {"),
     "bitmap_byte_must_be_one": ("if (mrow[kb] != 0) {", "if (mrow[kb] == 1) {"),
+    "kv_head_interleaved": ("(int64_t)b * Hkv + h / group;", "(int64_t)b * Hkv + h % Hkv;"),
+    "kv_head_stride_query_length": ("k + bkv * Sk * (int64_t)D", "k + bkv * Sq * (int64_t)D"),
+    "mask_row_stride_query_blocks": ("(int64_t)qb * nbk;", "(int64_t)qb * nbq;"),
 }
 
 

@@ -17,6 +17,10 @@ mistake is caught.
   pin_empty         empty rows: +0.0 (sign bit clear) and the finite sentinel
   pin_encodings     LUT -> bitmap -> attention is bit-identical to LUT -> attention;
                     bitmap <-> LUT conversions against Python set arithmetic
+  pin_gqa_cross     grouped-query heads (Hq = 3 Hkv) and Sq != Sk: dense selection equals
+                    fp64 scaled_dot_product_attention on K/V repeated per group; a tiny
+                    per-head sparse case equals the brute-force enumeration on the
+                    key/value head that each query head reads
 """
 import json
 import math
@@ -279,8 +283,56 @@ def pin_encodings(h):
         assert np.array_equal(o1, o4)
 
 
+def pin_gqa_cross(h):
+    # dense: every block selected, full blocks -> textbook attention with K/V heads
+    # repeated group-wise (query head hq reads key/value head hq // group)
+    B, Hq, Hkv, Sq, Sk, D, block = 2, 6, 2, 64, 160, 16, 16
+    nbq, nbk = Sq // block, Sk // block
+    q = _rand_bits((B, Hq, Sq, D), 801)
+    k, v = (_rand_bits((B, Hkv, Sk, D), 802 + i) for i in range(2))
+    idx = np.broadcast_to(np.arange(nbk, dtype=np.int32), (B, Hq, nbq, nbk)).copy()
+    num = np.full((B, Hq, nbq), nbk, np.int32)
+    scale = 0.29
+    out, lse = orc.vsa_forward(q, k, v, idx, num, None, block, scale, h=h)
+    out = out.reshape(B, Hq, Sq, D)
+    lse = lse.reshape(B, Hq, Sq)
+    tq, tk, tv = (torch.from_numpy(_bits_to_f64(x)) for x in (q, k, v))
+    tk = tk.repeat_interleave(Hq // Hkv, dim=1)
+    tv = tv.repeat_interleave(Hq // Hkv, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=scale)
+    ref_lse = torch.logsumexp(scale * tq @ tk.transpose(-1, -2), dim=-1) / math.log(2.0)
+    assert np.max(np.abs(out - ref.numpy())) <= 1e-12
+    assert np.max(np.abs(lse - ref_lse.numpy())) <= 1e-12
+    # sparse, per-head LUT over the key blocks, tail masks, more key than query blocks
+    rng = np.random.default_rng(11)
+    B, Hq, Hkv, Sq, Sk, D, block, max_kv = 1, 4, 2, 24, 56, 4, 8, 5
+    nbq, nbk = Sq // block, Sk // block
+    q = _rand_bits((B, Hq, Sq, D), 811, mul=1.5)
+    k, v = (_rand_bits((B, Hkv, Sk, D), 812 + i, mul=1.5) for i in range(2))
+    idx = rng.integers(-1, nbk + 1, size=(B, Hq, nbq, max_kv)).astype(np.int32)
+    num = rng.integers(0, max_kv + 1, size=(B, Hq, nbq)).astype(np.int32)
+    num[0, 1, 0] = 0
+    vbs = rng.integers(0, block + 1, size=nbk).astype(np.int32)
+    vbs[nbk - 1] = 3
+    out, lse = orc.vsa_forward(q, k, v, idx, num, vbs, block, 0.41, h=h)
+    out = out.reshape(B, Hq, Sq, D)
+    lse = lse.reshape(B, Hq, Sq)
+    qf, kf, vf = (_bits_to_f64(x) for x in (q, k, v))
+    for hq in range(Hq):
+        hk = hq // (Hq // Hkv)
+        for i in range(Sq):
+            qb = i // block
+            o, l = _brute_row(qf[0, hq], kf[0, hk], vf[0, hk], i, block, idx[0, hq, qb],
+                              int(num[0, hq, qb]), max_kv, vbs, 0.41)
+            if o is None:
+                assert np.all(out[0, hq, i] == 0.0) and lse[0, hq, i] == orc.LSE_EMPTY
+            else:
+                assert np.max(np.abs(out[0, hq, i] - o)) <= 1e-12
+                assert abs(lse[0, hq, i] - l) <= 1e-12
+
+
 PINS = [pin_golden, pin_dense, pin_bruteforce, pin_invariants, pin_closed_forms, pin_empty,
-        pin_encodings]
+        pin_encodings, pin_gqa_cross]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
