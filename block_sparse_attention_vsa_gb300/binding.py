@@ -6,8 +6,8 @@ CPU or eager-PyTorch fallback -- if the library is missing or was built for anot
 GPU the calls raise.
 
 Functions mirror the C entry points:
-  vsa_fwd, jenga_fwd, vsa_lut_to_bitmap, vsa_bitmap_to_lut, vsa_fwd_from_host,
-  vsa_device_status, vsa_workspace_bytes
+  vsa_fwd, vsa_fwd_gqa, vsa_fwd_from_mask, jenga_fwd, vsa_lut_to_bitmap,
+  vsa_bitmap_to_lut, vsa_fwd_from_host, vsa_device_status, vsa_workspace_bytes
 """
 from __future__ import annotations
 
@@ -28,7 +28,8 @@ MAX_BLOCKS = 2048
 # every symbol include/vsa.h declares
 EXPORTS = ("vsa_fwd", "jenga_fwd", "vsa_workspace_bytes", "vsa_lut_to_bitmap",
            "vsa_bitmap_to_lut", "vsa_fwd_from_host", "vsa_device_status",
-           "vsa_last_launch_count", "vsa_status_str", "vsa_fwd_noalloc")
+           "vsa_last_launch_count", "vsa_status_str", "vsa_fwd_noalloc", "vsa_fwd_gqa",
+           "vsa_fwd_from_mask")
 
 
 class VsaError(RuntimeError):
@@ -54,6 +55,12 @@ def load(path: str = LIB_PATH):
                           ctypes.c_uint)
     h.vsa_fwd.restype = i32
     h.vsa_fwd.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P, P, P]
+    h.vsa_fwd_gqa.restype = i32
+    h.vsa_fwd_gqa.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32, P,
+                              P, P, P]
+    h.vsa_fwd_from_mask.restype = i32
+    h.vsa_fwd_from_mask.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32,
+                                    P, P, P, P]
     h.jenga_fwd.restype = i32
     h.jenga_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P, P, P]
     h.vsa_fwd_noalloc.restype = i32
@@ -159,6 +166,77 @@ def vsa_fwd(q, k, v, q2k_idx, q2k_num, variable_block_sizes, block=None, scale=N
                      max_kv, block, scale, _ptr(out), _ptr(lse_t), _ptr(workspace),
                      _stream(stream))
     _check("vsa_fwd", code)
+    return out, lse_t
+
+
+def _qkv_gqa(q, k, v):
+    _dev(q, "q", torch.bfloat16, 4)
+    _dev(k, "k", torch.bfloat16, 4)
+    _dev(v, "v", torch.bfloat16, 4)
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    if v.shape != k.shape or Bk != B or Dk != D:
+        raise ValueError("k and v must be [B,Hkv,Sk,D] with q's B and D")
+    return B, Hq, Hkv, Sq, Sk, D
+
+
+def _lse_arg(lse, shape, device):
+    if lse is True:
+        return torch.empty(shape, dtype=torch.float32, device=device)
+    if lse is None or lse is False:
+        return None
+    return _dev(lse, "lse", torch.float32, 3)
+
+
+def vsa_fwd_gqa(q, k, v, q2k_idx, q2k_num, variable_block_sizes=None, block=64, scale=None,
+                out=None, lse=True, workspace=None, stream=None):
+    """Grouped-query / cross-length VSA forward.  q: bf16 [B,Hq,Sq,128]; k, v: bf16
+    [B,Hkv,Sk,128] (Hq a multiple of Hkv); q2k_idx [B,Hq,Sq/block,max_kv] with entries in
+    [0, Sk/block); q2k_num [B,Hq,Sq/block]; variable_block_sizes [Sk/block] or None."""
+    h = load()
+    B, Hq, Hkv, Sq, Sk, D = _qkv_gqa(q, k, v)
+    idx = _meta32(q2k_idx, "q2k_idx")
+    num = _meta32(q2k_num, "q2k_num")
+    nbq = Sq // block if block else 0
+    if idx.dim() != 4 or idx.shape[:3] != (B, Hq, nbq) or num.shape != (B, Hq, nbq):
+        raise ValueError("q2k_idx must be [B,Hq,Sq/block,max_kv] and q2k_num [B,Hq,Sq/block]")
+    vbs = None if variable_block_sizes is None else _meta32(variable_block_sizes,
+                                                             "variable_block_sizes")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else _dev(out, "out", torch.bfloat16, 4)
+    lse_t = _lse_arg(lse, (B, Hq, Sq), q.device)
+    code = h.vsa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(num), _ptr(vbs), B, Hq, Hkv,
+                         Sq, Sk, D, idx.shape[-1], block, scale, _ptr(out), _ptr(lse_t),
+                         _ptr(workspace), _stream(stream))
+    _check("vsa_fwd_gqa", code)
+    return out, lse_t
+
+
+def vsa_fwd_from_mask(q, k, v, block_map, variable_block_sizes=None, block=64, scale=None,
+                      out=None, lse=True, workspace=None, stream=None):
+    """Forward from a block map: bool/int8 [B,Hq,Sq/block,Sk/block] (one per query head) or
+    [Sq/block,Sk/block] (shared by every head).  Shapes otherwise as vsa_fwd_gqa."""
+    h = load()
+    B, Hq, Hkv, Sq, Sk, D = _qkv_gqa(q, k, v)
+    if block_map.dtype == torch.bool:
+        block_map = block_map.to(torch.int8)
+    _dev(block_map, "block_map", torch.int8)
+    nbq, nbk = (Sq // block, Sk // block) if block else (0, 0)
+    if tuple(block_map.shape) == (nbq, nbk):
+        shared = 1
+    elif tuple(block_map.shape) == (B, Hq, nbq, nbk):
+        shared = 0
+    else:
+        raise ValueError("block_map must be [B,Hq,Sq/block,Sk/block] or [Sq/block,Sk/block]")
+    vbs = None if variable_block_sizes is None else _meta32(variable_block_sizes,
+                                                             "variable_block_sizes")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else _dev(out, "out", torch.bfloat16, 4)
+    lse_t = _lse_arg(lse, (B, Hq, Sq), q.device)
+    code = h.vsa_fwd_from_mask(_ptr(q), _ptr(k), _ptr(v), _ptr(block_map), shared, _ptr(vbs), B,
+                               Hq, Hkv, Sq, Sk, D, block, scale, _ptr(out), _ptr(lse_t),
+                               _ptr(workspace), _stream(stream))
+    _check("vsa_fwd_from_mask", code)
     return out, lse_t
 
 

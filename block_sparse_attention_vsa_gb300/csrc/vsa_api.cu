@@ -123,6 +123,22 @@ bool make_map(CUtensorMap* m, const void* ptr, long long rows, int box_rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view [heads, seq, 128] of a BHSD bf16 tensor, box {64, 128, 1}: a box that runs
+// past the end of a head's sequence is clipped there (loads read zeros, stores drop the
+// rows) instead of spilling into the next head.
+bool make_map_3d(CUtensorMap* m, const void* ptr, long long heads, long long seq) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)seq, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {128 * 2, (cuuint64_t)seq * 128 * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb_) {
@@ -130,9 +146,70 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb_) {
   return x < y + nb_ && y < x + na;
 }
 
+// Problem shape shared by every forward entry point: q / out [B, Hq, Sq, D],
+// k / v [B, Hkv, Sk, D], lse [B, Hq, Sq].
+struct Shape {
+  int B, Hq, Hkv, Sq, Sk, D, block;
+  float scale;
+  long long rows_q() const { return (long long)B * Hq * Sq; }
+  long long rows_k() const { return (long long)B * Hkv * Sk; }
+};
+
+// Host-side checks of a forward call (no device reads).  `nothing` is set when there is
+// no output row to write.
+vsa_status check_shape(const void* q, const void* k, const void* v, const void* out,
+                       const float* lse, const Shape& p, DeviceInfo** dev, bool* nothing) {
+  *nothing = false;
+  if (p.B < 0 || p.Hq < 0 || p.Hkv < 0 || p.Sq < 0 || p.Sk < 0) return VSA_ERR_INVALID_ARG;
+  if (p.D != VSA_HEAD_DIM) return VSA_ERR_UNSUPPORTED;
+  if (p.block != 64 && p.block != 128) return VSA_ERR_UNSUPPORTED;
+  if (!(p.scale > 0.0f) || !std::isfinite(p.scale)) return VSA_ERR_INVALID_ARG;
+  if (p.Sq % p.block != 0 || p.Sk % p.block != 0) return VSA_ERR_INVALID_ARG;
+  if (p.Hq > 0 && (p.Hkv < 1 || p.Hq % p.Hkv != 0)) return VSA_ERR_INVALID_ARG;
+  if (p.Sk / p.block > VSA_MAX_BLOCKS) return VSA_ERR_UNSUPPORTED;
+  if (p.rows_q() > (long long)INT_MAX || p.rows_k() > (long long)INT_MAX)
+    return VSA_ERR_UNSUPPORTED;
+  if (p.rows_q() == 0) {
+    *nothing = true;
+    return VSA_OK;
+  }
+  const bool keys = p.rows_k() > 0;
+  if (!q || !out || (keys && (!k || !v))) return VSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || (keys && (!aligned16(k) || !aligned16(v))))
+    return VSA_ERR_INVALID_ARG;
+  const size_t qbytes = (size_t)p.rows_q() * p.D * 2, kbytes = (size_t)p.rows_k() * p.D * 2;
+  if (overlaps(out, qbytes, q, qbytes) ||
+      (keys && (overlaps(out, qbytes, k, kbytes) || overlaps(out, qbytes, v, kbytes))))
+    return VSA_ERR_INVALID_ARG;
+  if (lse && overlaps(lse, (size_t)p.rows_q() * 4, out, qbytes)) return VSA_ERR_INVALID_ARG;
+  vsa_status st = device_info(dev);
+  if (st != VSA_OK) return st;
+  if ((*dev)->major != 10 || (*dev)->minor != 3) return VSA_ERR_UNSUPPORTED;
+  return VSA_OK;
+}
+
+// FwdArgs fields that follow from the shape alone.
+FwdArgs shape_args(const Shape& p, float* lse, void* workspace, unsigned int* status) {
+  FwdArgs a{};
+  a.lse = lse;
+  a.sched = static_cast<unsigned int*>(workspace);
+  a.status = status;
+  a.Hq = p.Hq;
+  a.Hkv = p.Hkv;
+  a.group = p.Hq / p.Hkv;
+  a.Sq = p.Sq;
+  a.Sk = p.Sk;
+  a.nbq = p.Sq / p.block;
+  a.nbk = p.Sk / p.block;
+  a.items_per_bh = p.block == 64 ? (a.nbq + 1) / 2 : a.nbq;
+  a.n_items = (int)((long long)p.B * p.Hq * a.items_per_bh);
+  a.scale_log2 = p.scale * 1.4426950408889634f;
+  return a;
+}
+
 template <int BLOCK, bool JENGA>
 vsa_status launch_fwd(DeviceInfo* dev, int slot, const void* q, const void* k, const void* v,
-                      void* out, long long rows, const FwdArgs& args, cudaStream_t stream) {
+                      void* out, const Shape& p, const FwdArgs& args, cudaStream_t stream) {
   auto kern = bsa_fwd_kernel<BLOCK, JENGA>;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -149,9 +226,14 @@ vsa_status launch_fwd(DeviceInfo* dev, int slot, const void* q, const void* k, c
   // The kernel moves registers between warpgroups (setmaxnreg); the launch must provide
   // the pool that re-balancing draws on, or a warpgroup would wait for registers forever.
   if ((long long)dev->regs[slot] * kThreads < (long long)kRegPoolNeeded) return VSA_ERR_UNSUPPORTED;
+  // With no keys at all (Sk == 0) no K/V copy is ever issued; the maps only need to encode.
+  const bool keys = p.rows_k() > 0;
+  const void* kp = keys ? k : q;
+  const void* vp = keys ? v : q;
+  const long long krows = keys ? p.rows_k() : p.rows_q();
   CUtensorMap tq, tk, tv, to;
-  if (!make_map(&tq, q, rows, 128) || !make_map(&tk, k, rows, BLOCK) ||
-      !make_map(&tv, v, rows, BLOCK) || !make_map(&to, out, rows, 128))
+  if (!make_map_3d(&tq, q, (long long)p.B * p.Hq, p.Sq) || !make_map(&tk, kp, krows, BLOCK) ||
+      !make_map(&tv, vp, krows, BLOCK) || !make_map_3d(&to, out, (long long)p.B * p.Hq, p.Sq))
     return VSA_ERR_CUDA;
   const int ctas = (args.n_items + 1) / 2;  // two work items in flight per CTA
   const int grid = ctas < dev->sm_count ? ctas : dev->sm_count;
@@ -161,35 +243,65 @@ vsa_status launch_fwd(DeviceInfo* dev, int slot, const void* q, const void* k, c
   return VSA_OK;
 }
 
-vsa_status common_checks(const void* q, const void* k, const void* v, const void* out, int B,
-                         int H, int S, int D, int block, float scale, DeviceInfo** dev,
-                         bool* nothing) {
-  *nothing = false;
-  if (B < 0 || H < 0 || S < 0) return VSA_ERR_INVALID_ARG;
-  if (D != VSA_HEAD_DIM) return VSA_ERR_UNSUPPORTED;
-  if (block != 64 && block != 128) return VSA_ERR_UNSUPPORTED;
-  if (!(scale > 0.0f) || !std::isfinite(scale)) return VSA_ERR_INVALID_ARG;
-  if (S % block != 0) return VSA_ERR_INVALID_ARG;
-  const int nb = S / block;
-  if (nb % 2 != 0) return VSA_ERR_UNSUPPORTED;
-  if (nb > VSA_MAX_BLOCKS) return VSA_ERR_UNSUPPORTED;
-  const long long rows = (long long)B * H * S;
-  if (rows > (long long)INT_MAX) return VSA_ERR_UNSUPPORTED;
-  if (rows == 0) {
-    *nothing = true;
-    return VSA_OK;
-  }
-  if (!q || !k || !v || !out) return VSA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
-    return VSA_ERR_INVALID_ARG;
-  const size_t bytes = (size_t)rows * D * 2;
-  if (overlaps(out, bytes, q, bytes) || overlaps(out, bytes, k, bytes) ||
-      overlaps(out, bytes, v, bytes))
-    return VSA_ERR_INVALID_ARG;
-  vsa_status st = device_info(dev);
-  if (st != VSA_OK) return st;
-  if ((*dev)->major != 10 || (*dev)->minor != 3) return VSA_ERR_UNSUPPORTED;
-  return VSA_OK;
+unsigned int* status_word() {
+  unsigned int* status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_status) != cudaSuccess)
+    return nullptr;
+  return status;
+}
+
+bool workspace_ok(const void* workspace) {
+  return workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 3u) == 0;
+}
+
+// LUT-driven forward (VSA), any head grouping and lengths.
+vsa_status run_lut(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
+                   const int32_t* q2k_idx, const int32_t* q2k_num, const int32_t* vbs,
+                   const Shape& p, int max_kv, vsa_bf16* out, float* lse, void* workspace,
+                   vsa_stream_t stream, bool require_vbs) {
+  t_last_launches = 0;
+  DeviceInfo* dev = nullptr;
+  bool nothing = false;
+  vsa_status st = check_shape(q, k, v, out, lse, p, &dev, &nothing);
+  if (st != VSA_OK || nothing) return st;
+  if (max_kv < 1) return VSA_ERR_INVALID_ARG;
+  if (!q2k_idx || !q2k_num || (require_vbs && !vbs)) return VSA_ERR_INVALID_ARG;
+  if (!workspace_ok(workspace)) return VSA_ERR_INVALID_ARG;
+  unsigned int* status = status_word();
+  if (status == nullptr) return VSA_ERR_CUDA;
+  FwdArgs a = shape_args(p, lse, workspace, status);
+  a.q2k_idx = q2k_idx;
+  a.q2k_num = q2k_num;
+  a.vbs = vbs;
+  a.max_kv = max_kv;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p.block == 64) return launch_fwd<64, false>(dev, 0, q, k, v, out, p, a, s);
+  return launch_fwd<128, false>(dev, 1, q, k, v, out, p, a, s);
+}
+
+// Block-map-driven forward: one int8 map per (b, hq) (bh_stride = nbq * nbk) or one map
+// shared by all of them (bh_stride = 0); the kernel compacts each map row itself.
+vsa_status run_map(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
+                   const int8_t* block_map, long long bh_stride, const int32_t* vbs,
+                   const Shape& p, vsa_bf16* out, float* lse, void* workspace,
+                   vsa_stream_t stream) {
+  t_last_launches = 0;
+  DeviceInfo* dev = nullptr;
+  bool nothing = false;
+  vsa_status st = check_shape(q, k, v, out, lse, p, &dev, &nothing);
+  if (st != VSA_OK || nothing) return st;
+  if (!block_map) return VSA_ERR_INVALID_ARG;
+  if (!workspace_ok(workspace)) return VSA_ERR_INVALID_ARG;
+  unsigned int* status = status_word();
+  if (status == nullptr) return VSA_ERR_CUDA;
+  FwdArgs a = shape_args(p, lse, workspace, status);
+  a.bitmap = block_map;
+  a.bitmap_bh_stride = bh_stride;
+  a.vbs = vbs;
+  a.max_kv = 1;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p.block == 64) return launch_fwd<64, true>(dev, 2, q, k, v, out, p, a, s);
+  return launch_fwd<128, true>(dev, 3, q, k, v, out, p, a, s);
 }
 
 }  // namespace
@@ -203,38 +315,19 @@ vsa_status vsa_fwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
                    const int32_t* variable_block_sizes, int B, int H, int S, int D, int max_kv,
                    int block, float scale, vsa_bf16* out, float* lse, void* workspace,
                    vsa_stream_t stream) {
-  t_last_launches = 0;
-  DeviceInfo* dev = nullptr;
-  bool nothing = false;
-  vsa_status st = common_checks(q, k, v, out, B, H, S, D, block, scale, &dev, &nothing);
-  if (st != VSA_OK || nothing) return st;
-  if (max_kv < 1) return VSA_ERR_INVALID_ARG;
-  if (!q2k_idx || !q2k_num || !variable_block_sizes) return VSA_ERR_INVALID_ARG;
-  if (lse && overlaps(lse, (size_t)B * H * S * 4, out, (size_t)B * H * S * D * 2))
-    return VSA_ERR_INVALID_ARG;
-  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 3u)) return VSA_ERR_INVALID_ARG;
-  const int nb = S / block;
-  FwdArgs a{};
-  a.q2k_idx = q2k_idx;
-  a.q2k_num = q2k_num;
-  a.vbs = variable_block_sizes;
-  a.bitmap = nullptr;
-  a.lse = lse;
-  a.sched = static_cast<unsigned int*>(workspace);
-  unsigned int* status = nullptr;
-  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_status) != cudaSuccess)
-    return VSA_ERR_CUDA;
-  a.status = status;
-  a.H = H;
-  a.S = S;
-  a.nb = nb;
-  a.max_kv = max_kv;
-  a.n_items = (int)((long long)B * H * nb / (block == 64 ? 2 : 1));
-  a.scale_log2 = scale * 1.4426950408889634f;
-  const long long rows = (long long)B * H * S;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (block == 64) return launch_fwd<64, false>(dev, 0, q, k, v, out, rows, a, s);
-  return launch_fwd<128, false>(dev, 1, q, k, v, out, rows, a, s);
+  const Shape p{B, H, H, S, S, D, block, scale};
+  return run_lut(q, k, v, q2k_idx, q2k_num, variable_block_sizes, p, max_kv, out, lse,
+                 workspace, stream, true);
+}
+
+vsa_status vsa_fwd_gqa(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
+                       const int32_t* q2k_idx, const int32_t* q2k_num,
+                       const int32_t* variable_block_sizes, int B, int Hq, int Hkv, int Sq,
+                       int Sk, int D, int max_kv, int block, float scale, vsa_bf16* out,
+                       float* lse, void* workspace, vsa_stream_t stream) {
+  const Shape p{B, Hq, Hkv, Sq, Sk, D, block, scale};
+  return run_lut(q, k, v, q2k_idx, q2k_num, variable_block_sizes, p, max_kv, out, lse,
+                 workspace, stream, false);
 }
 
 vsa_status jenga_fwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
@@ -243,34 +336,20 @@ vsa_status jenga_fwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
                      vsa_stream_t stream) {
   t_last_launches = 0;
   if (block_q != block_k) return VSA_ERR_UNSUPPORTED;
-  DeviceInfo* dev = nullptr;
-  bool nothing = false;
-  vsa_status st = common_checks(q, k, v, out, B, H, S, D, block_k, scale, &dev, &nothing);
-  if (st != VSA_OK || nothing) return st;
-  if (!mask_bitmap) return VSA_ERR_INVALID_ARG;
-  if (lse && overlaps(lse, (size_t)B * H * S * 4, out, (size_t)B * H * S * D * 2))
-    return VSA_ERR_INVALID_ARG;
-  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 3u)) return VSA_ERR_INVALID_ARG;
-  const int block = block_k;
-  const int nb = S / block;
-  FwdArgs a{};
-  a.bitmap = mask_bitmap;
-  a.lse = lse;
-  a.sched = static_cast<unsigned int*>(workspace);
-  unsigned int* status = nullptr;
-  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_status) != cudaSuccess)
-    return VSA_ERR_CUDA;
-  a.status = status;
-  a.H = H;
-  a.S = S;
-  a.nb = nb;
-  a.max_kv = 1;
-  a.n_items = (int)((long long)B * H * nb / (block == 64 ? 2 : 1));
-  a.scale_log2 = scale * 1.4426950408889634f;
-  const long long rows = (long long)B * H * S;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (block == 64) return launch_fwd<64, true>(dev, 2, q, k, v, out, rows, a, s);
-  return launch_fwd<128, true>(dev, 3, q, k, v, out, rows, a, s);
+  const Shape p{B, H, H, S, S, D, block_k, scale};
+  return run_map(q, k, v, mask_bitmap, 0, nullptr, p, out, lse, workspace, stream);
+}
+
+vsa_status vsa_fwd_from_mask(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
+                             const int8_t* block_map, int map_shared,
+                             const int32_t* variable_block_sizes, int B, int Hq, int Hkv,
+                             int Sq, int Sk, int D, int block, float scale, vsa_bf16* out,
+                             float* lse, void* workspace, vsa_stream_t stream) {
+  const Shape p{B, Hq, Hkv, Sq, Sk, D, block, scale};
+  const long long stride =
+      map_shared ? 0 : (block > 0 ? (long long)(Sq / block) * (Sk / block) : 0);
+  return run_map(q, k, v, block_map, stride, variable_block_sizes, p, out, lse, workspace,
+                 stream);
 }
 
 vsa_status vsa_lut_to_bitmap(const int32_t* q2k_idx, const int32_t* q2k_num, int rows,
@@ -319,7 +398,9 @@ vsa_status vsa_fwd_from_host(const vsa_bf16* h_q, const vsa_bf16* h_k, const vsa
   // validate the device-side arguments before any copy is enqueued
   DeviceInfo* dev = nullptr;
   bool nothing = false;
-  vsa_status st = common_checks(d_q, d_k, d_v, d_out, B, H, S, D, block, scale, &dev, &nothing);
+  const Shape shape{B, H, H, S, S, D, block, scale};
+  vsa_status st =
+      check_shape(d_q, d_k, d_v, d_out, h_lse ? d_lse : nullptr, shape, &dev, &nothing);
   if (st != VSA_OK) return st;
   if (!d_q2k_idx || !d_q2k_num || !d_variable_block_sizes) return VSA_ERR_INVALID_ARG;
   if (cudaMemcpyAsync(d_q, h_q, tbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
@@ -375,12 +456,11 @@ vsa_status noalloc_checks(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* 
                           int block, float scale, const vsa_bf16* out, const float* lse,
                           bool* nothing) {
   DeviceInfo* dev = nullptr;
-  vsa_status st = common_checks(q, k, v, out, B, H, S, D, block, scale, &dev, nothing);
+  const Shape p{B, H, H, S, S, D, block, scale};
+  vsa_status st = check_shape(q, k, v, out, lse, p, &dev, nothing);
   if (st != VSA_OK || *nothing) return st;
   if (max_kv < 1) return VSA_ERR_INVALID_ARG;
   if (!q2k_idx || !q2k_num || !vbs) return VSA_ERR_INVALID_ARG;
-  if (lse && overlaps(lse, (size_t)B * H * S * 4, out, (size_t)B * H * S * D * 2))
-    return VSA_ERR_INVALID_ARG;
   return VSA_OK;
 }
 }  // namespace

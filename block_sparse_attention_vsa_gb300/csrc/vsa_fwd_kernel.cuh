@@ -97,15 +97,20 @@ struct SmemCtl {
 };
 static_assert(sizeof(SmemCtl) <= kCtlBytes, "control block too large");
 
+// Shapes: q / out [B, Hq, Sq, 128], k / v [B, Hkv, Sk, 128]; query head hq of batch b
+// reads key/value head b*Hkv + hq / group.  nbq = Sq / BLOCK query blocks, nbk = Sk / BLOCK
+// key blocks; a work item is one query block (BLOCK 128) or an adjacent pair (BLOCK 64,
+// the last item of a head holding a single block when nbq is odd).
 struct FwdArgs {
-  const int32_t* q2k_idx;  // VSA
-  const int32_t* q2k_num;
-  const int32_t* vbs;
-  const int8_t* bitmap;    // Jenga
-  float* lse;              // may be null
+  const int32_t* q2k_idx;  // LUT mode: [B*Hq*nbq, max_kv]
+  const int32_t* q2k_num;  //           [B*Hq*nbq]
+  const int32_t* vbs;      // [nbk] valid keys per key block, or null = every block full
+  const int8_t* bitmap;    // bitmap mode: [nbq, nbk] rows, (b*Hq + hq) * bitmap_bh_stride apart
+  long long bitmap_bh_stride;  // 0 = one map shared by every (b, hq)
+  float* lse;              // [B*Hq*Sq] or null
   unsigned int* sched;     // null = static schedule; else {next item, CTAs done}
   unsigned int* status;    // device status word
-  int H, S, nb, max_kv, n_items;
+  int Hq, Hkv, group, Sq, Sk, nbq, nbk, max_kv, n_items, items_per_bh;
   float scale_log2;
 };
 
@@ -156,7 +161,7 @@ __device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
   uint8_t* bm1 = bm0 + kMaxNb;
   const uint64_t pol_kv = policy_evict_last();
   const uint64_t pol_q = policy_evict_first();
-  const int nb = a.nb;
+  const int nb = a.nbk;
   uint32_t L = 0;                            // K/V tiles loaded so far (ring position)
   uint32_t fills[kStages] = {0, 0, 0, 0};    // copies issued per ring stage
   uint32_t qfills[2] = {0, 0};               // Q copies issued per Q buffer
@@ -176,14 +181,16 @@ __device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
     if (it >= 2 && !wait_bar(&ctl->list_empty[buf], ((it >> 1) + 1) & 1, ctl, a.status, 1)) break;
     uint32_t* list = reinterpret_cast<uint32_t*>(smem + kOffList) + buf * kMaxNb;
     int count = 0, bh = 0, qa = 0;
+    bool pair = false;  // the item's second query block exists
     if (item >= 0) {
-      const int items_per_bh = nb / C::kPairs;
-      bh = item / items_per_bh;
-      qa = (item - bh * items_per_bh) * C::kPairs;
+      bh = item / a.items_per_bh;
+      qa = (item - bh * a.items_per_bh) * C::kPairs;
+      pair = C::kPairs == 2 && qa + 1 < a.nbq;
       if (!JENGA) {
 #pragma unroll
         for (int hf = 0; hf < C::kPairs; ++hf) {
-          const long long row = (long long)bh * nb + qa + hf;
+          if (hf == 1 && !pair) break;
+          const long long row = (long long)bh * a.nbq + qa + hf;
           int n = a.q2k_num[row];
           n = n < 0 ? 0 : (n > a.max_kv ? a.max_kv : n);
           const int32_t* lut = a.q2k_idx + row * a.max_kv;
@@ -200,8 +207,9 @@ __device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
         uint32_t h0 = 0, h1 = 0;
         if (kb < nb) {
           if (JENGA) {
-            h0 = a.bitmap[(long long)qa * nb + kb] != 0;
-            if (C::kPairs == 2) h1 = a.bitmap[(long long)(qa + 1) * nb + kb] != 0;
+            const int8_t* mrow = a.bitmap + bh * a.bitmap_bh_stride + (long long)qa * nb;
+            h0 = mrow[kb] != 0;
+            if (pair) h1 = mrow[nb + kb] != 0;
           } else {
             h0 = bm0[kb];
             if (C::kPairs == 2) h1 = bm1[kb];
@@ -212,7 +220,7 @@ __device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
         if (sel) {
           const int pos = count + __popc(ballot & ((1u << lane) - 1u));
           int valid = BLOCK;
-          if (!JENGA) {
+          if (a.vbs != nullptr) {
             valid = a.vbs[kb];
             valid = valid < 0 ? 0 : (valid > BLOCK ? BLOCK : valid);
           }
@@ -237,12 +245,14 @@ __device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
     if (it >= 2 && !wait_bar(&ctl->q_empty[buf], ((it >> 1) + 1) & 1, ctl, a.status, 2)) break;
     const int n_tiles = (count + C::kSub - 1) / C::kSub;
     if (n_tiles == 0) continue;
-    const int row0 = bh * a.S + qa * BLOCK;
+    // key/value head of this query head (grouped-query attention)
+    const int kvh = (bh / a.Hq) * a.Hkv + (bh % a.Hq) / a.group;
     uint8_t* qs = smem + kOffQ + buf * kTileBytes;
     if (lane == 0) {
+      // 128 query rows of head bh; rows past Sq (a lone last block) read as zeros
       mbar_arrive_expect_tx(&ctl->q_full[buf], kTileBytes);
-      tma_load_2d_hint(qs, tq, &ctl->q_full[buf], 0, row0, pol_q);
-      tma_load_2d_hint(qs + kTileBytes / 2, tq, &ctl->q_full[buf], 64, row0, pol_q);
+      tma_load_3d_hint(qs, tq, &ctl->q_full[buf], 0, qa * BLOCK, bh, pol_q);
+      tma_load_3d_hint(qs + kTileBytes / 2, tq, &ctl->q_full[buf], 64, qa * BLOCK, bh, pol_q);
     }
     ++qfills[buf];
     // K/V tiles in the order the MMA warp consumes them: K0, K1, V0, K2, V1, ...
@@ -264,7 +274,7 @@ __device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
         if (lane == 0) {
           mbar_arrive_expect_tx(&ctl->kv_full[stage], (uint32_t)ne * BLOCK * 128 * 2);
           for (int e = 0; e < ne; ++e) {
-            const int krow = bh * a.S + (int)(list[e0 + e] & 0xFFFFu) * BLOCK;
+            const int krow = kvh * a.Sk + (int)(list[e0 + e] & 0xFFFFu) * BLOCK;
             // d-halves are separate [128 rows][64] sub-tiles; block e fills rows e*BLOCK..
             tma_load_2d_hint(dst + e * BLOCK * 128, map, &ctl->kv_full[stage], 0, krow, pol_kv);
             tma_load_2d_hint(dst + kTileBytes / 2 + e * BLOCK * 128, map, &ctl->kv_full[stage],
@@ -570,10 +580,8 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
     // accumulator may still hold an earlier item's values)
     const bool use0 = __any_sync(0xffffffffu, lr[0] > 0.0f);
     const bool use1 = __any_sync(0xffffffffu, lr[1] > 0.0f);
-    const int items_per_bh = a.nb / C::kPairs;
-    const int bh = item / items_per_bh;
-    const int qa = (item - bh * items_per_bh) * C::kPairs;
-    const int row0 = bh * a.S + qa * BLOCK;
+    const int bh = item / a.items_per_bh;
+    const int qa = (item - bh * a.items_per_bh) * C::kPairs;
     uint8_t* qs = smem + kOffQ + buf * kTileBytes + w * (kTileBytes / 2);
 #pragma unroll 1
     for (int cc = 0; cc < 4; ++cc) {  // this warpgroup's 64 output columns, 16 at a time
@@ -606,8 +614,8 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
                      : "memory");
       }
     }
-    if (w == 0 && a.lse != nullptr)
-      a.lse[(long long)row0 + row] = has ? mm + log2f(l_e) : -3.402823466e+38f;
+    if (w == 0 && a.lse != nullptr && qa * BLOCK + row < a.Sq)
+      a.lse[(long long)bh * a.Sq + qa * BLOCK + row] = has ? mm + log2f(l_e) : -3.402823466e+38f;
     tc_fence_before();
     fence_proxy_async_smem();
     __syncwarp();
@@ -619,7 +627,7 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
     if (n_tiles > 0) ++ne_items;
     if (leader) {
       if (!wait_bar(&ctl->epi_bar[w], it & 1, ctl, a.status, 24)) break;
-      tma_store_2d(to, qs, w * 64, row0);
+      tma_store_3d(to, qs, w * 64, qa * BLOCK, bh);  // rows past Sq are not written
       bulk_commit_group();
       bulk_wait_group_read0();
       mbar_arrive(&ctl->q_empty[buf]);

@@ -27,6 +27,11 @@ The five workloads:
                   to it (squared Euclidean distance, ties by id, itself included)
                   plus 16 distinct random others (128 = 8.3 %);
                   variable_block_sizes 64 except the last block, 32
+
+Grouped-query / cross-length and block-map cases (make_random_gqa) draw q as
+[B, Hq, Sq, 128] and k, v as [B, Hkv, Sk, 128] in the same order and way; their LUT
+rows pick distinct random key blocks of [0, Sk/block), and the block-map form is the
+0/1 expansion of those rows (one int8 map per (b, hq)).
 """
 from __future__ import annotations
 
@@ -57,10 +62,27 @@ class Workload:
     vbs: np.ndarray | None = None       # int32 [nb]
     bitmap: np.ndarray | None = None    # int8 [nb,nb] (jenga)
     extra: dict = field(default_factory=dict)
+    Hkv: int | None = None              # key/value heads (None = H)
+    Sk: int | None = None               # key length (None = S)
+    block_map: np.ndarray | None = None  # int8 [B,H,nbq,nbk] or [nbq,nbk] ("mask" kind)
+
+    def __post_init__(self):
+        if self.Hkv is None:
+            self.Hkv = self.H
+        if self.Sk is None:
+            self.Sk = self.S
 
     @property
     def nb(self) -> int:
         return self.S // self.block
+
+    @property
+    def nbq(self) -> int:
+        return self.S // self.block
+
+    @property
+    def nbk(self) -> int:
+        return self.Sk // self.block
 
     @property
     def max_kv(self) -> int:
@@ -240,6 +262,41 @@ def make_random_vsa(B, H, S, D, block, max_kv, seed, n_lo=0, n_hi=None, vbs_lo=N
         vbs = torch.randint(vbs_lo, vbs_hi + 1, (nb,), generator=g).to(torch.int32).numpy()
     return Workload("random_vsa", "vsa", B, H, S, D, block, 1.0 / math.sqrt(D), q, k, v,
                     q2k_idx=idx, q2k_num=num, vbs=vbs)
+
+
+def make_random_gqa(B, Hq, Hkv, Sq, Sk, D, block, max_kv, seed, n_lo=0, n_hi=None,
+                    vbs_lo=None, vbs_hi=None, kind="vsa", shared_map=False,
+                    qk_mul=1.0) -> Workload:
+    """Grouped-query / cross-length case: q [B,Hq,Sq,D], k and v [B,Hkv,Sk,D].  kind "vsa"
+    carries the LUT (rows over the Sk/block key blocks); kind "mask" carries the same
+    selection as an int8 block map [B,Hq,nbq,nbk], or with ``shared_map`` the map of
+    (b=0, hq=0) alone as [nbq,nbk] for every head."""
+    nbq, nbk = Sq // block, Sk // block
+    n_hi = min(max_kv, nbk) if n_hi is None else n_hi
+    g = gen(seed)
+    q = randn_bf16((B, Hq, Sq, D), g, qk_mul)
+    k = randn_bf16((B, Hkv, Sk, D), g, qk_mul)
+    v = randn_bf16((B, Hkv, Sk, D), g)
+    counts = torch.randint(n_lo, n_hi + 1, (B, Hq, nbq), generator=g)
+    keys = torch.rand((B, Hq, nbq, max(nbk, 1)), generator=g)[..., :nbk]
+    idx = _rows_from_ranks(keys, counts, max_kv)
+    num = counts.to(torch.int32).numpy()
+    if vbs_lo is None:
+        vbs = np.full(nbk, block, dtype=np.int32)
+    else:
+        vbs = torch.randint(vbs_lo, vbs_hi + 1, (nbk,), generator=g).to(torch.int32).numpy()
+    w = Workload("random_gqa", kind, B, Hq, Sq, D, block, 1.0 / math.sqrt(D), q, k, v,
+                 q2k_idx=idx, q2k_num=num, vbs=vbs, Hkv=Hkv, Sk=Sk)
+    if kind == "mask":
+        bm = np.zeros((B, Hq, nbq, nbk), dtype=np.int8)
+        slot = np.arange(max_kv)
+        for b in range(B):
+            for h in range(Hq):
+                for qb in range(nbq):
+                    row = idx[b, h, qb][slot < num[b, h, qb]]
+                    bm[b, h, qb, row] = 1
+        w.block_map = np.ascontiguousarray(bm[0, 0]) if shared_map else bm
+    return w
 
 
 def bits(t: torch.Tensor) -> np.ndarray:

@@ -57,7 +57,7 @@ typedef enum vsa_status {
   VSA_OK = 0,
   VSA_ERR_INVALID_ARG = 1,    /* null pointer, bad shape, misaligned tensor, bad scale */
   VSA_ERR_UNSUPPORTED = 2,    /* valid but not built for: D != 128, block not 64/128,
-                                 odd block count, too many blocks, device not sm_103 */
+                                 too many key blocks, device not sm_103 */
   VSA_ERR_CUDA = 3,           /* a CUDA runtime call failed (launch, copy, attribute) */
   VSA_ERR_DEVICE_TIMEOUT = 4  /* a kernel gave up on an internal wait (vsa_device_status) */
 } vsa_status;
@@ -66,7 +66,7 @@ typedef enum vsa_status {
  * -FLT_MAX, the most negative finite binary32. */
 #define VSA_LSE_EMPTY (-FLT_MAX)
 #define VSA_HEAD_DIM 128
-/* Largest number of key blocks per sequence (S / block) the kernels accept. */
+/* Largest number of key blocks per sequence (Sk / block) the kernels accept. */
 #define VSA_MAX_BLOCKS 2048
 
 /* every entry point is exported from the shared library */
@@ -87,7 +87,9 @@ typedef struct CUstream_st *vsa_stream_t; /* == cudaStream_t */
  *   q2k_num      [B, H, nb] int32 valid-entry counts (0 allowed).
  *   variable_block_sizes  [nb] int32, each in [0, block]: valid keys of each key block;
  *                keys at positions >= it are masked (values are clamped to [0, block]).
- *   block        64 or 128 tokens per block; S must be a multiple, nb = S / block even.
+ *   block        64 or 128 tokens per block; S must be a multiple.  (The FastVideo
+ *                contract asks for an even nb; an odd nb is accepted as well: with block
+ *                64 the last query block of each head is then computed on its own.)
  *   scale        natural-exp softmax scale (finite, > 0), typically 1/sqrt(D).
  *   out          [B, H, S, D] bf16 output; must not overlap any input.
  *   lse          [B, H, S] fp32 output (base 2), or NULL to skip it (need_lse = false).
@@ -106,8 +108,8 @@ VSA_API vsa_status vsa_fwd(const vsa_bf16 *q, const vsa_bf16 *k, const vsa_bf16 
 
 /* Jenga forward: the selection is one i8 bitmap mask_bitmap[S/block_q, S/block_k],
  * shared by every batch and head; a nonzero byte means attend.  Every key of a selected
- * block is valid (no tail mask).  block_q == block_k, 64 or 128; S a multiple of it with
- * an even block count.  Other arguments as vsa_fwd.
+ * block is valid (no tail mask).  block_q == block_k, 64 or 128; S a multiple of it.
+ * Other arguments as vsa_fwd.
  * Source: "TheRock rocke sparse_attention.py", module docstring (Jenga bullet),
  * _stage_jenga_mask_to_lds, _lds_bitmap_predicate, build_jenga_sparse_attention. */
 VSA_API vsa_status jenga_fwd(const vsa_bf16 *q, const vsa_bf16 *k, const vsa_bf16 *v,
@@ -115,7 +117,47 @@ VSA_API vsa_status jenga_fwd(const vsa_bf16 *q, const vsa_bf16 *k, const vsa_bf1
                      int block_k, float scale, vsa_bf16 *out, float *lse, void *workspace,
                      vsa_stream_t stream);
 
-/* Bytes of device workspace vsa_fwd / jenga_fwd use when given one. */
+/* Grouped-query and cross-length VSA forward: vsa_fwd with separate query / key-value
+ * head counts and sequence lengths.
+ *   q, out       [B, Hq, Sq, D] bf16;  k, v  [B, Hkv, Sk, D] bf16;  Hq a multiple of Hkv.
+ *                Query head hq reads key/value head hq / (Hq / Hkv).
+ *   q2k_idx      [B, Hq, Sq/block, max_kv] int32, entries in [0, Sk/block).
+ *   q2k_num      [B, Hq, Sq/block] int32.
+ *   variable_block_sizes  [Sk/block] int32, or NULL for full key blocks.
+ *   lse          [B, Hq, Sq] fp32 or NULL.
+ *   Sq and Sk are multiples of block; Sk / block <= VSA_MAX_BLOCKS.  Sk = 0 is allowed:
+ *   every row is then empty (out 0, lse VSA_LSE_EMPTY).  Hq % Hkv != 0 is
+ *   VSA_ERR_INVALID_ARG.  Other arguments and errors as vsa_fwd; with Hq = Hkv = H and
+ *   Sq = Sk = S this is vsa_fwd.
+ * Source: "TheRock rocke sparse_attention.py", JengaSparseSpec / VsaSparseSpec (separate
+ * seqlen_q, seqlen_k and query / key-value head counts; the key-value head of a query
+ * head, kv_head_idx). */
+VSA_API vsa_status vsa_fwd_gqa(const vsa_bf16 *q, const vsa_bf16 *k, const vsa_bf16 *v,
+                               const int32_t *q2k_idx, const int32_t *q2k_num,
+                               const int32_t *variable_block_sizes, int B, int Hq, int Hkv,
+                               int Sq, int Sk, int D, int max_kv, int block, float scale,
+                               vsa_bf16 *out, float *lse, void *workspace, vsa_stream_t stream);
+
+/* Forward straight from a block map, compacted inside the kernel (no LUT is built in
+ * memory).
+ *   block_map    int8, nonzero = attend.  map_shared == 0: [B, Hq, Sq/block, Sk/block],
+ *                one map per (batch, query head); map_shared != 0: [Sq/block, Sk/block],
+ *                one map for every batch and head (the Jenga layout).
+ *   variable_block_sizes  [Sk/block] int32 valid keys per key block, or NULL = full.
+ *   Shapes, lse, workspace and errors as vsa_fwd_gqa.  The result equals vsa_fwd_gqa on
+ *   the LUT that vsa_bitmap_to_lut makes from the same map with max_kv = Sk/block.
+ * Source: "FastVideo block_sparse_attn_sm100a.py", _block_sparse_attn_sm100a_from_mask_
+ * inference and block_sparse_attn_sm100a_from_mask (a bool block_map [B, H, nb, nb] turned
+ * into the forward's selection); "TheRock rocke sparse_attention.py", Jenga bullet of the
+ * module docstring (an i8 map, nonzero = attend). */
+VSA_API vsa_status vsa_fwd_from_mask(const vsa_bf16 *q, const vsa_bf16 *k, const vsa_bf16 *v,
+                                     const int8_t *block_map, int map_shared,
+                                     const int32_t *variable_block_sizes, int B, int Hq,
+                                     int Hkv, int Sq, int Sk, int D, int block, float scale,
+                                     vsa_bf16 *out, float *lse, void *workspace,
+                                     vsa_stream_t stream);
+
+/* Bytes of device workspace the forward entry points use when given one. */
 VSA_API size_t vsa_workspace_bytes(void);
 
 /* Size of the library's own scheduling scratch used by vsa_fwd_noalloc. */
@@ -182,8 +224,8 @@ VSA_API vsa_status vsa_fwd_from_host(const vsa_bf16 *h_q, const vsa_bf16 *h_k, c
  * last call (`detail`, if not NULL, receives the recorded code). */
 VSA_API vsa_status vsa_device_status(vsa_stream_t stream, unsigned int *detail);
 
-/* Number of kernel launches the most recent successful vsa_fwd / jenga_fwd call on
- * this thread enqueued (for accounting in benchmarks). */
+/* Number of kernel launches the most recent successful forward call on this thread
+ * enqueued (for accounting in benchmarks). */
 VSA_API int vsa_last_launch_count(void);
 
 /* Static text for a status code. */

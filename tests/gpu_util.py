@@ -22,6 +22,9 @@ def to_dev(w):
         r["idx"] = torch.from_numpy(np.ascontiguousarray(w.q2k_idx)).to(d)
         r["num"] = torch.from_numpy(np.ascontiguousarray(w.q2k_num)).to(d)
         r["vbs"] = torch.from_numpy(np.ascontiguousarray(w.vbs)).to(d)
+    elif w.kind == "mask":
+        r["map"] = torch.from_numpy(np.ascontiguousarray(w.block_map)).to(d)
+        r["vbs"] = torch.from_numpy(np.ascontiguousarray(w.vbs)).to(d)
     else:
         r["bitmap"] = torch.from_numpy(np.ascontiguousarray(w.bitmap)).to(d)
     return r
@@ -29,7 +32,16 @@ def to_dev(w):
 
 def run_gpu(w, dev=None, lse=True, workspace=None):
     dev = dev or to_dev(w)
-    if w.kind == "vsa":
+    gqa = w.Hkv != w.H or w.Sk != w.S
+    if w.kind == "vsa" and gqa:
+        out, l = binding.vsa_fwd_gqa(dev["q"], dev["k"], dev["v"], dev["idx"], dev["num"],
+                                     dev["vbs"], block=w.block, scale=w.scale, lse=lse,
+                                     workspace=workspace)
+    elif w.kind == "mask":
+        out, l = binding.vsa_fwd_from_mask(dev["q"], dev["k"], dev["v"], dev["map"], dev["vbs"],
+                                           block=w.block, scale=w.scale, lse=lse,
+                                           workspace=workspace)
+    elif w.kind == "vsa":
         out, l = binding.vsa_fwd(dev["q"], dev["k"], dev["v"], dev["idx"], dev["num"], dev["vbs"],
                                  block=w.block, scale=w.scale, lse=lse, workspace=workspace)
     else:
@@ -45,6 +57,9 @@ def run_oracle(w, sel=None):
     qb, kb, vb = workloads.bits(w.q), workloads.bits(w.k), workloads.bits(w.v)
     if w.kind == "vsa":
         return orc.vsa_forward(qb, kb, vb, w.q2k_idx, w.q2k_num, w.vbs, w.block, w.scale, sel=sel)
+    if w.kind == "mask":
+        return orc.masked_attention(qb, kb, vb, w.block_map, w.block, w.scale, vbs=w.vbs,
+                                    sel=sel)
     return orc.jenga_forward(qb, kb, vb, w.bitmap, w.block, w.scale, sel=sel)
 
 
@@ -55,7 +70,7 @@ def gather_rows(t, sel, block):
 
 
 def compare(w, out, lse, sel=None):
-    sel = orc.all_qblocks(w.B, w.H, w.nb) if sel is None else np.asarray(sel, np.int32)
+    sel = orc.all_qblocks(w.B, w.H, w.nbq) if sel is None else np.asarray(sel, np.int32)
     ref_o, ref_l = run_oracle(w, sel)
     o = gather_rows(out, sel, w.block).astype(np.float64)
     err = np.abs(o - ref_o)

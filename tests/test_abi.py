@@ -66,7 +66,6 @@ def _fwd(lib, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(D=64), binding.VSA_ERR_UNSUPPORTED),
     (dict(block=32), binding.VSA_ERR_UNSUPPORTED),
-    (dict(S=64 * 3), binding.VSA_ERR_UNSUPPORTED),        # odd number of blocks
     (dict(S=100), binding.VSA_ERR_INVALID_ARG),           # not a multiple of the block
     (dict(S=64 * 4096), binding.VSA_ERR_UNSUPPORTED),     # more than VSA_MAX_BLOCKS blocks
     (dict(scale=0.0), binding.VSA_ERR_INVALID_ARG),
@@ -86,6 +85,46 @@ def test_jenga_requires_square_blocks(lib):
     P = ctypes.c_void_p
     code = lib.jenga_fwd(P(1 << 20), P(2 << 20), P(3 << 20), P(4 << 20), 1, 1, 256, 128, 64, 128,
                          0.088, P(5 << 20), None, None, None)
+    assert code == binding.VSA_ERR_UNSUPPORTED
+
+
+def _gqa(lib, **kw):
+    args = dict(B=1, Hq=4, Hkv=2, Sq=256, Sk=384, D=128, max_kv=4, block=64, vbs=6 << 20)
+    args.update(kw)
+    P = ctypes.c_void_p
+    return lib.vsa_fwd_gqa(P(1 << 20), P(2 << 20), P(3 << 20), P(4 << 20), P(5 << 20),
+                           P(args["vbs"]) if args["vbs"] else None, args["B"], args["Hq"],
+                           args["Hkv"], args["Sq"], args["Sk"], args["D"], args["max_kv"],
+                           args["block"], 0.088, P(7 << 20), None, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hkv=3), binding.VSA_ERR_INVALID_ARG),           # Hq not a multiple of Hkv
+    (dict(Hkv=0), binding.VSA_ERR_INVALID_ARG),
+    (dict(Sk=100), binding.VSA_ERR_INVALID_ARG),          # Sk not a multiple of the block
+    (dict(Sq=96), binding.VSA_ERR_INVALID_ARG),
+    (dict(Sk=64 * 4096), binding.VSA_ERR_UNSUPPORTED),    # too many key blocks
+    (dict(D=64), binding.VSA_ERR_UNSUPPORTED),
+    (dict(max_kv=0), binding.VSA_ERR_CUDA),               # shape checks pass, then no device
+])
+def test_gqa_host_validation_without_gpu(lib, kw, code):
+    got = _gqa(lib, **kw)
+    if code == binding.VSA_ERR_CUDA:
+        # without a GPU the device query fails first; with one, max_kv = 0 is rejected
+        assert got in (binding.VSA_ERR_CUDA, binding.VSA_ERR_INVALID_ARG)
+    else:
+        assert got == code
+
+
+def test_gqa_and_mask_empty_problems(lib):
+    assert _gqa(lib, Sq=0) == binding.VSA_OK
+    assert _gqa(lib, B=0) == binding.VSA_OK
+    P = ctypes.c_void_p
+    code = lib.vsa_fwd_from_mask(P(1 << 20), P(2 << 20), P(3 << 20), None, 0, None, 1, 2, 2, 0,
+                                 256, 128, 64, 0.088, P(7 << 20), None, None, None)
+    assert code == binding.VSA_OK
+    code = lib.vsa_fwd_from_mask(P(1 << 20), P(2 << 20), P(3 << 20), P(4 << 20), 0, None, 1, 2,
+                                 2, 256, 256, 128, 48, 0.088, P(7 << 20), None, None, None)
     assert code == binding.VSA_ERR_UNSUPPORTED
 
 
