@@ -80,12 +80,16 @@ constexpr unsigned kErrTimeout = 0x100u;  // | code of the wait that gave up
 struct SmemCtl {
   uint64_t list_full[2], list_empty[2];
   uint64_t q_full[2], q_empty[2];
+  // kv_full[s]: ring stage s holds its tile.  kv_empty[s]: the MMAs that read the
+  // stage's tile have completed.  The MMA warp commits kv_empty right after a tile's QK
+  // (K stage) and after its PV (V stage), so the same phases also tell the softmax warps
+  // that S is ready (K stage) and that O is up to date (V stage).  A stage is reused
+  // every kStages ring positions, and the tile loaded there next cannot be consumed
+  // before every waiter has moved on, so no waiter is ever two phases behind.
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2];   // S buffer b holds a fresh tile
-  uint64_t p_full[2][2];  // [w][b]: warpgroup w has written its P half of S buffer b
-                          // (per buffer, so a warp running a tile ahead of its siblings
-                          // can never complete the previous tile's phase)
-  uint64_t pv_done[2];  // warpgroup w's PV half has completed
+  uint64_t p_full[2];   // all 8 softmax warps have written P into S buffer b (per buffer,
+                        // so a warp running a tile ahead can never complete the previous
+                        // tile's phase)
   uint64_t o_full, o_empty;
   uint64_t stats_bar[2];
   uint64_t epi_bar[2];
@@ -304,8 +308,7 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
   constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);
   uint32_t L = 0;            // ring position
   uint32_t g = 0;            // key tiles issued so far, across items (S buffer g & 1)
-  uint32_t gw[2] = {0, 0};   // PV halves issued per warpgroup (PV-done phases)
-  uint32_t pc[2][2] = {{0, 0}, {0, 0}};  // P phases per (warpgroup, S buffer)
+  uint32_t pc[2] = {0, 0};   // P phases per S buffer
   uint32_t ne_items = 0;     // non-empty items so far (O phases)
   uint32_t nq[2] = {0, 0};   // Q fills consumed per Q buffer
   for (uint32_t it = 0;; ++it) {
@@ -343,8 +346,7 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
           const uint64_t off16 = ((k >> 2) * (kTileBytes / 2) + (k & 3) * 32) >> 4;
           mma_ss(tS, qdesc + off16, kdesc + off16, idesc, k > 0);
         }
-        mma_commit(&ctl->kv_empty[stage]);
-        mma_commit(&ctl->s_full[sb]);
+        mma_commit(&ctl->kv_empty[stage]);  // K stage free; S ready
         ++L;
       }
       if (t >= 1) {  // O_w += P V for the previous tile, one key half per warpgroup
@@ -365,27 +367,24 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
             smem_desc_sw128(smem_addr(smem + kOffKV + stage * kTileBytes), kTileBytes / 2, 1024);
         const uint32_t pb = (g + tp) & 1;
         const uint32_t tS = tmem + kColS + pb * 128;
+        if (!wait_bar(&ctl->p_full[pb], pc[pb] & 1, ctl, a.status, 14)) {
+          ok = false;
+          break;
+        }
+        ++pc[pb];
+        tc_fence_after();
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
           if (w >= halves) break;
-          if (!wait_bar(&ctl->p_full[w][pb], pc[w][pb] & 1, ctl, a.status, 14)) {
-            ok = false;
-            break;
-          }
-          ++pc[w][pb];
-          tc_fence_after();
           const uint32_t tO = tmem + kColO + w * 128;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             mma_ts(tO, tS + w * 64 + k * 8, vdesc + ((w * 8192 + k * 2048) >> 4), kIdescPV,
                    (!first[w] || k > 0) ? 1u : 0u);
           }
-          mma_commit(&ctl->pv_done[w]);
           first[w] = false;
-          ++gw[w];
         }
-        if (!ok) break;
-        mma_commit(&ctl->kv_empty[stage]);
+        mma_commit(&ctl->kv_empty[stage]);  // V stage free; O holds this tile
         ++L;
       }
     }
@@ -479,7 +478,7 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
   float* stats = reinterpret_cast<float*>(smem + kOffStats);  // [par][wg][3][128]
   const bool leader = row == 0;
   uint32_t g = 0;         // key tiles seen so far, across items (S buffer g & 1)
-  uint32_t gw = 0;        // tiles this warpgroup took part in (P / PV phases)
+  uint32_t ring = 0;      // ring position of the current item's first K tile
   uint32_t ne_items = 0;
   for (uint32_t it = 0;; ++it) {
     const uint32_t buf = it & 1;
@@ -495,16 +494,22 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
     for (int t = 0; t < n_tiles; ++t, ++g) {
       const int e0 = t * C::kSub;
       const int ne = (count - e0) < C::kSub ? (count - e0) : C::kSub;
-      if (ne * BLOCK / 64 <= w) continue;  // a 64-key tile has no second half
-      int lim;
-      if (BLOCK == 64) {
-        lim = entry_limit(list[e0 + w], half);
-      } else {
-        lim = entry_limit(list[e0], half) - 64 * w;
-        lim = lim < 0 ? 0 : (lim > 64 ? 64 : lim);
+      // A 64-key tile has no second half: warpgroup 1 then writes nothing, but still
+      // waits for the tile and arrives, so that every P phase takes all 8 warps.
+      const bool has_half = ne * BLOCK / 64 > w;
+      int lim = 0;
+      if (has_half) {
+        if (BLOCK == 64) {
+          lim = entry_limit(list[e0 + w], half);
+        } else {
+          lim = entry_limit(list[e0], half) - 64 * w;
+          lim = lim < 0 ? 0 : (lim > 64 ? 64 : lim);
+        }
       }
       const uint32_t sb = g & 1;
-      if (!wait_bar(&ctl->s_full[sb], (g >> 1) & 1, ctl, a.status, 21)) {
+      // ring order K0, K1, V0, K2, V1, ...: K(t) sits at t ? 2t - 1 : 0, V(t) at 2t + 2
+      const uint32_t kpos = ring + (t ? 2u * t - 1u : 0u);
+      if (!wait_bar(&ctl->kv_empty[kpos % kStages], (kpos / kStages) & 1, ctl, a.status, 21)) {
         ok = false;
         break;
       }
@@ -513,7 +518,7 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
       float alpha = 1.0f;
       if (lim > 0) {
         softmax_tile<64>(tS, lim, 64, 64, a.scale_log2, m_run, l_exact, l_round, alpha);
-      } else {
+      } else if (has_half) {
         // none of this warp's rows attends these keys (a block selected only by the other
         // query block of the pair, or a zero-width tail): P = 0, the running state stays.
         // lim depends only on the row's query half, so the branch is warp-uniform.
@@ -522,10 +527,11 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
         for (int j = 0; j < 32; ++j) z[j] = 0u;
         tmem_st_32x32b_x32(tS, z);
       }
-      // O rescale when this row's reference max moved: wait until this warpgroup's
-      // previous PV has completed (TMEM access is warp-collective, hence the vote).
+      // O rescale when this row's reference max moved: wait until the previous tile's PV
+      // has completed (TMEM access is warp-collective, hence the vote).
       if (__any_sync(0xffffffffu, alpha != 1.0f) && started) {
-        if (!wait_bar(&ctl->pv_done[w], (gw - 1) & 1, ctl, a.status, 25)) {
+        const uint32_t vpos = ring + 2u * t;  // V(t - 1)
+        if (!wait_bar(&ctl->kv_empty[vpos % kStages], (vpos / kStages) & 1, ctl, a.status, 25)) {
           ok = false;
           break;
         }
@@ -543,11 +549,11 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->p_full[w][sb]);
-      ++gw;
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->p_full[sb]);
       started = true;
     }
     if (!ok) break;
+    ring += 2u * (uint32_t)n_tiles;  // the item's K and V tiles
     // ---- merge the two halves of the key walk, then this warpgroup's half of the output
     float* st = stats + buf * (2 * 3 * 128);
     st[(w * 3 + 0) * 128 + row] = m_run;
@@ -653,10 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->list_empty[i], 9);  // the MMA thread + 8 softmax warps
       mbar_init(&ctl->q_full[i], 1);
       mbar_init(&ctl->q_empty[i], 2);     // one TMA-store leader per softmax warpgroup
-      mbar_init(&ctl->s_full[i], 1);
-      mbar_init(&ctl->p_full[i][0], 4);
-      mbar_init(&ctl->p_full[i][1], 4);
-      mbar_init(&ctl->pv_done[i], 1);
+      mbar_init(&ctl->p_full[i], 8);
       mbar_init(&ctl->stats_bar[i], 8);
       mbar_init(&ctl->epi_bar[i], 4);
     }
