@@ -17,16 +17,19 @@
 //              tile (N = 128; the last tile of an odd union has N = 64).
 //
 // Structure: one persistent CTA per SM, 12 warps.
-//   warp 8      producer: per work item, turns the LUT rows (or Jenga bitmap rows) into
-//               an ascending list of selected key blocks -- an SMEM byte-map scatter then
-//               a ballot/popc compaction, so repeated or out-of-range LUT entries can
-//               never cause a duplicate or an out-of-bounds copy -- then TMA-loads Q
-//               (double-buffered across items) and ONLY the selected K/V blocks into a
-//               4-stage ring, in the order the MMA warp consumes them.
+//   warp 10     lists: per work item, one item ahead of its use, turns the LUT rows (or
+//               block-map rows) into the list of selected key blocks -- an SMEM byte-map
+//               scatter then a ballot/popc compaction, so repeated or out-of-range LUT
+//               entries can never cause a duplicate or an out-of-bounds copy.  Block-64
+//               lists put blocks only one query block selects in alternating pairs first
+//               (see build_list).  Lists are double-buffered.
+//   warp 8      TMA: Q (double-buffered across items) and ONLY the selected K/V blocks
+//               into a 4-stage ring, in the order the MMA warp consumes them.
 //   warp 9      MMA issuer (one thread): S_g = Q K_g^T into TMEM S buffer g%2 (g counts
 //               key tiles across items), then, per key half w, O_w += P_g[:, 64w:64w+64]
 //               V_g[64w:64w+64, :] with P read from TMEM.  Issue order QK0, QK1, PV0,
-//               QK2, PV1, ..., so QK_{t+1} runs while P_t is computed.
+//               QK2, PV1, ..., so QK_{t+1} runs while P_t is computed.  Two commits per
+//               tile release the K and the V ring stage (see SmemCtl).
 //   warps 0-3   softmax warpgroup 0: keys 0-63 of every key tile;
 //   warps 4-7   softmax warpgroup 1: keys 64-127 of every key tile.  One thread per
 //               query row; each warpgroup keeps its own running max m (log2 domain,
@@ -35,7 +38,7 @@
 //               loop.  After the item they merge (m, l, O) of both halves and each
 //               warpgroup normalises, stages and TMA-stores one 64-column half of the
 //               output; warpgroup 0 writes lse.
-//   warps 10-11 idle.
+//   warp 11     idle.
 // TMEM (512 columns): S0, S1 at columns 0, 128 (warpgroup w reads S columns 64w..64w+63
 // and writes its bf16 P over the first 32 of them); O0, O1 at 256, 384.
 // Every mbarrier wait is bounded; a wait that runs out records a code in the device
@@ -55,7 +58,7 @@ constexpr int kMaxNb = 2048;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per wait
 constexpr float kRescaleThreshold = 8.0f;         // log2 units: stale max allowed to lag 2^8
 constexpr uint32_t kSoftmaxRegs = 216;            // per thread, softmax warpgroups
-constexpr uint32_t kOtherRegs = 56;               // per thread, producer/MMA warpgroup
+constexpr uint32_t kOtherRegs = 56;               // per thread, TMA / MMA / list warps
 // registers the launch must provide for the re-balancing above (checked on the host)
 constexpr uint32_t kRegPoolNeeded = 256 * kSoftmaxRegs + 128 * kOtherRegs;
 
@@ -155,140 +158,236 @@ struct Cfg {
 // ------------------------------------------------------------------------------------
 // producer warp: work items, block lists, TMA copies
 // ------------------------------------------------------------------------------------
+struct ItemHead {
+  int item, count, bh, qa;
+};
+
+// Pick the CTA's it-th work item, build its key-block list into list buffer it & 1 and
+// publish the header (item -1 = no more work).  `ok` turns false if a wait gave up.
+template <int BLOCK, bool JENGA>
+__device__ ItemHead build_list(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t it,
+                               bool& ok) {
+  using C = Cfg<BLOCK>;
+  const uint32_t lane = lane_id();
+  uint8_t* bm0 = smem + kOffBm;
+  uint8_t* bm1 = bm0 + kMaxNb;
+  const int nb = a.nbk;
+  const uint32_t buf = it & 1;
+  ItemHead h{-1, 0, 0, 0};
+  if (a.sched == nullptr) {
+    const long long s = (long long)blockIdx.x + (long long)it * gridDim.x;
+    h.item = s < a.n_items ? (int)s : -1;
+  } else {
+    unsigned got = 0;
+    if (lane == 0) got = atomicAdd(&a.sched[0], 1u);
+    got = __shfl_sync(0xffffffffu, got, 0);
+    h.item = got < (unsigned)a.n_items ? (int)got : -1;
+  }
+  if (it >= 2 && !wait_bar(&ctl->list_empty[buf], ((it >> 1) + 1) & 1, ctl, a.status, 1)) {
+    ok = false;
+    return h;
+  }
+  uint32_t* list = reinterpret_cast<uint32_t*>(smem + kOffList) + buf * kMaxNb;
+  int count = 0;
+  if (h.item >= 0) {
+    h.bh = h.item / a.items_per_bh;
+    h.qa = (h.item - h.bh * a.items_per_bh) * C::kPairs;
+    const bool pair = C::kPairs == 2 && h.qa + 1 < a.nbq;  // the second query block exists
+    // the item's selection as byte maps (which start, and are always left, all zero)
+    if (!JENGA) {
+#pragma unroll
+      for (int hf = 0; hf < C::kPairs; ++hf) {
+        if (hf == 1 && !pair) break;
+        const long long row = (long long)h.bh * a.nbq + h.qa + hf;
+        int n = a.q2k_num[row];
+        n = n < 0 ? 0 : (n > a.max_kv ? a.max_kv : n);
+        const int32_t* lut = a.q2k_idx + row * a.max_kv;
+        uint8_t* bm = hf ? bm1 : bm0;
+        for (int s = lane; s < n; s += 32) {
+          const int kb = lut[s];
+          if (kb >= 0 && kb < nb) bm[kb] = 1;
+        }
+      }
+    } else {
+      const int8_t* mrow = a.bitmap + h.bh * a.bitmap_bh_stride + (long long)h.qa * nb;
+      for (int base = 0; base < nb; base += 128) {
+        int8_t v0[4], v1[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int kb = base + 32 * j + (int)lane;
+          v0[j] = kb < nb ? mrow[kb] : 0;
+          v1[j] = (pair && kb < nb) ? mrow[nb + kb] : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int kb = base + 32 * j + (int)lane;
+          if (kb < nb) {
+            bm0[kb] = v0[j] != 0;
+            if (C::kPairs == 2) bm1[kb] = v1[j] != 0;
+          }
+        }
+      }
+    }
+    __syncwarp();
+    // which query block(s) select key block kb (bit 0: the first, bit 1: the second)
+    auto selected = [&](int kb) -> uint32_t {
+      if (kb >= nb) return 0u;
+      return (uint32_t)bm0[kb] | (C::kPairs == 2 ? (uint32_t)bm1[kb] << 1 : 0u);
+    };
+    auto valid_keys = [&](int kb) -> int {
+      int valid = BLOCK;
+      if (a.vbs != nullptr) {
+        valid = a.vbs[kb];
+        valid = valid < 0 ? 0 : (valid > BLOCK ? BLOCK : valid);
+      }
+      return valid;
+    };
+    const uint32_t below = (1u << lane) - 1u;
+    if (C::kPairs == 1) {
+      // ascending compaction
+      for (int base = 0; base < nb; base += 32) {
+        const int kb = base + (int)lane;
+        const uint32_t sel = selected(kb);
+        const uint32_t ballot = __ballot_sync(0xffffffffu, sel != 0);
+        if (sel) {
+          list[count + __popc(ballot & below)] = make_entry(kb, 3u, valid_keys(kb));
+          bm0[kb] = 0;
+        }
+        count += __popc(ballot);
+      }
+    } else {
+      // Block-64 pairs.  A key tile is two consecutive entries, one per softmax
+      // warpgroup; the first query block's rows sit on two SM sub-partitions, the
+      // second's on the other two.  A tile pairing a block only the first query block
+      // selected (X) with one only the second selected (Y) gives every sub-partition one
+      // busy softmax warp instead of two busy and two idle, so the list is laid out as
+      // min(|X|, |Y|) XY tiles first, then the remaining X or Y, then the blocks both
+      // select (each kind ascending).  The order changes only the summation order.
+      int nx = 0, ny = 0;
+      for (int base = 0; base < nb; base += 32) {
+        const uint32_t sel = selected(base + (int)lane);
+        nx += __popc(__ballot_sync(0xffffffffu, sel == 1u));
+        ny += __popc(__ballot_sync(0xffffffffu, sel == 2u));
+      }
+      const int xy = nx < ny ? nx : ny;
+      const int rest = (nx - xy) + (ny - xy);
+      int cx = 0, cy = 0, cb = 0;
+      for (int base = 0; base < nb; base += 32) {
+        const int kb = base + (int)lane;
+        const uint32_t sel = selected(kb);
+        const uint32_t bx = __ballot_sync(0xffffffffu, sel == 1u);
+        const uint32_t by = __ballot_sync(0xffffffffu, sel == 2u);
+        const uint32_t bb = __ballot_sync(0xffffffffu, sel == 3u);
+        if (sel) {
+          int pos;
+          if (sel == 1u) {
+            const int i = cx + __popc(bx & below);
+            pos = i < xy ? 2 * i : 2 * xy + (i - xy);
+          } else if (sel == 2u) {
+            const int i = cy + __popc(by & below);
+            pos = i < xy ? 2 * i + 1 : 2 * xy + (i - xy);
+          } else {
+            pos = 2 * xy + rest + cb + __popc(bb & below);
+          }
+          list[pos] = make_entry(kb, sel, valid_keys(kb));
+          bm0[kb] = 0;
+          bm1[kb] = 0;
+        }
+        cx += __popc(bx);
+        cy += __popc(by);
+        cb += __popc(bb);
+      }
+      count = nx + ny + cb;
+    }
+    __syncwarp();
+  }
+  h.count = count;
+  if (lane == 0) {
+    ctl->hdr_item[buf] = h.item;
+    ctl->hdr_n[buf] = count;
+    mbar_arrive(&ctl->list_full[buf]);
+  }
+  __syncwarp();
+  return h;
+}
+
+// List warp: builds the CTA's work items' lists one item ahead of their use.
+template <int BLOCK, bool JENGA>
+__device__ void list_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a) {
+  bool ok = true;
+  for (uint32_t it = 0; ok; ++it)
+    if (build_list<BLOCK, JENGA>(smem, ctl, a, it, ok).item < 0) break;
+}
+
+// TMA warp: Q and the selected K/V tiles of each item, in the order the MMA consumes them.
 template <int BLOCK, bool JENGA>
 __device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
                               const CUtensorMap* tq, const CUtensorMap* tk,
                               const CUtensorMap* tv) {
   using C = Cfg<BLOCK>;
   const uint32_t lane = lane_id();
-  uint8_t* bm0 = smem + kOffBm;
-  uint8_t* bm1 = bm0 + kMaxNb;
   const uint64_t pol_kv = policy_evict_last();
   const uint64_t pol_q = policy_evict_first();
-  const int nb = a.nbk;
   uint32_t L = 0;                            // K/V tiles loaded so far (ring position)
   uint32_t fills[kStages] = {0, 0, 0, 0};    // copies issued per ring stage
   uint32_t qfills[2] = {0, 0};               // Q copies issued per Q buffer
   bool ok = true;
   for (uint32_t it = 0; ok; ++it) {
     const uint32_t buf = it & 1;
-    int item;
-    if (a.sched == nullptr) {
-      const long long s = (long long)blockIdx.x + (long long)it * gridDim.x;
-      item = s < a.n_items ? (int)s : -1;
-    } else {
-      unsigned got = 0;
-      if (lane == 0) got = atomicAdd(&a.sched[0], 1u);
-      got = __shfl_sync(0xffffffffu, got, 0);
-      item = got < (unsigned)a.n_items ? (int)got : -1;
-    }
-    if (it >= 2 && !wait_bar(&ctl->list_empty[buf], ((it >> 1) + 1) & 1, ctl, a.status, 1)) break;
-    uint32_t* list = reinterpret_cast<uint32_t*>(smem + kOffList) + buf * kMaxNb;
-    int count = 0, bh = 0, qa = 0;
-    bool pair = false;  // the item's second query block exists
-    if (item >= 0) {
-      bh = item / a.items_per_bh;
-      qa = (item - bh * a.items_per_bh) * C::kPairs;
-      pair = C::kPairs == 2 && qa + 1 < a.nbq;
-      if (!JENGA) {
-#pragma unroll
-        for (int hf = 0; hf < C::kPairs; ++hf) {
-          if (hf == 1 && !pair) break;
-          const long long row = (long long)bh * a.nbq + qa + hf;
-          int n = a.q2k_num[row];
-          n = n < 0 ? 0 : (n > a.max_kv ? a.max_kv : n);
-          const int32_t* lut = a.q2k_idx + row * a.max_kv;
-          uint8_t* bm = hf ? bm1 : bm0;
-          for (int s = lane; s < n; s += 32) {
-            const int kb = lut[s];
-            if (kb >= 0 && kb < nb) bm[kb] = 1;
-          }
-        }
-        __syncwarp();
-      }
-      for (int base = 0; base < nb; base += 32) {
-        const int kb = base + (int)lane;
-        uint32_t h0 = 0, h1 = 0;
-        if (kb < nb) {
-          if (JENGA) {
-            const int8_t* mrow = a.bitmap + bh * a.bitmap_bh_stride + (long long)qa * nb;
-            h0 = mrow[kb] != 0;
-            if (pair) h1 = mrow[nb + kb] != 0;
-          } else {
-            h0 = bm0[kb];
-            if (C::kPairs == 2) h1 = bm1[kb];
-          }
-        }
-        const uint32_t sel = h0 | h1;
-        const uint32_t ballot = __ballot_sync(0xffffffffu, sel != 0);
-        if (sel) {
-          const int pos = count + __popc(ballot & ((1u << lane) - 1u));
-          int valid = BLOCK;
-          if (a.vbs != nullptr) {
-            valid = a.vbs[kb];
-            valid = valid < 0 ? 0 : (valid > BLOCK ? BLOCK : valid);
-          }
-          list[pos] = make_entry(kb, (C::kPairs == 2) ? (h0 | (h1 << 1)) : 3u, valid);
-          if (!JENGA) {
-            bm0[kb] = 0;
-            if (C::kPairs == 2) bm1[kb] = 0;
-          }
-        }
-        count += __popc(ballot);
-      }
-      __syncwarp();
-    }
-    if (lane == 0) {
-      ctl->hdr_item[buf] = item;
-      ctl->hdr_n[buf] = count;
-      mbar_arrive(&ctl->list_full[buf]);
-    }
-    __syncwarp();
+    if (!wait_bar(&ctl->list_full[buf], (it >> 1) & 1, ctl, a.status, 7)) break;
+    const int item = ctl->hdr_item[buf];
+    const int count = ctl->hdr_n[buf];
     if (item < 0) break;
+    const uint32_t* list = reinterpret_cast<const uint32_t*>(smem + kOffList) + buf * kMaxNb;
+    const int bh = item / a.items_per_bh;
+    const int qa = (item - bh * a.items_per_bh) * C::kPairs;
     // Q (also the item's output staging buffer): free once the item two back is stored
     if (it >= 2 && !wait_bar(&ctl->q_empty[buf], ((it >> 1) + 1) & 1, ctl, a.status, 2)) break;
     const int n_tiles = (count + C::kSub - 1) / C::kSub;
-    if (n_tiles == 0) continue;
-    // key/value head of this query head (grouped-query attention)
-    const int kvh = (bh / a.Hq) * a.Hkv + (bh % a.Hq) / a.group;
-    uint8_t* qs = smem + kOffQ + buf * kTileBytes;
-    if (lane == 0) {
-      // 128 query rows of head bh; rows past Sq (a lone last block) read as zeros
-      mbar_arrive_expect_tx(&ctl->q_full[buf], kTileBytes);
-      tma_load_3d_hint(qs, tq, &ctl->q_full[buf], 0, qa * BLOCK, bh, pol_q);
-      tma_load_3d_hint(qs + kTileBytes / 2, tq, &ctl->q_full[buf], 64, qa * BLOCK, bh, pol_q);
-    }
-    ++qfills[buf];
-    // K/V tiles in the order the MMA warp consumes them: K0, K1, V0, K2, V1, ...
-    for (int t = 0; t <= n_tiles && ok; ++t) {
+    if (n_tiles > 0) {
+      // key/value head of this query head (grouped-query attention)
+      const int kvh = (bh / a.Hq) * a.Hkv + (bh % a.Hq) / a.group;
+      uint8_t* qs = smem + kOffQ + buf * kTileBytes;
+      if (lane == 0) {
+        // 128 query rows of head bh; rows past Sq (a lone last block) read as zeros
+        mbar_arrive_expect_tx(&ctl->q_full[buf], kTileBytes);
+        tma_load_3d_hint(qs, tq, &ctl->q_full[buf], 0, qa * BLOCK, bh, pol_q);
+        tma_load_3d_hint(qs + kTileBytes / 2, tq, &ctl->q_full[buf], 64, qa * BLOCK, bh, pol_q);
+      }
+      ++qfills[buf];
+      // K/V tiles in the order the MMA warp consumes them: K0, K1, V0, K2, V1, ...
+      for (int t = 0; t <= n_tiles && ok; ++t) {
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {  // 0: K of tile t, 1: V of tile t-1
-        const int tt = which == 0 ? t : t - 1;
-        if (tt < 0 || tt >= n_tiles) continue;
-        const uint32_t stage = L % kStages;
-        if (L >= kStages &&
-            !wait_bar(&ctl->kv_empty[stage], ((L / kStages) + 1) & 1, ctl, a.status, 3)) {
-          ok = false;
-          break;
-        }
-        const CUtensorMap* map = which == 0 ? tk : tv;
-        uint8_t* dst = smem + kOffKV + stage * kTileBytes;
-        const int e0 = tt * C::kSub;
-        const int ne = (count - e0) < C::kSub ? (count - e0) : C::kSub;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&ctl->kv_full[stage], (uint32_t)ne * BLOCK * 128 * 2);
-          for (int e = 0; e < ne; ++e) {
-            const int krow = kvh * a.Sk + (int)(list[e0 + e] & 0xFFFFu) * BLOCK;
-            // d-halves are separate [128 rows][64] sub-tiles; block e fills rows e*BLOCK..
-            tma_load_2d_hint(dst + e * BLOCK * 128, map, &ctl->kv_full[stage], 0, krow, pol_kv);
-            tma_load_2d_hint(dst + kTileBytes / 2 + e * BLOCK * 128, map, &ctl->kv_full[stage],
-                             64, krow, pol_kv);
+        for (int which = 0; which < 2; ++which) {  // 0: K of tile t, 1: V of tile t-1
+          const int tt = which == 0 ? t : t - 1;
+          if (tt < 0 || tt >= n_tiles) continue;
+          const uint32_t stage = L % kStages;
+          if (L >= kStages &&
+              !wait_bar(&ctl->kv_empty[stage], ((L / kStages) + 1) & 1, ctl, a.status, 3)) {
+            ok = false;
+            break;
           }
+          const CUtensorMap* map = which == 0 ? tk : tv;
+          uint8_t* dst = smem + kOffKV + stage * kTileBytes;
+          const int e0 = tt * C::kSub;
+          const int ne = (count - e0) < C::kSub ? (count - e0) : C::kSub;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&ctl->kv_full[stage], (uint32_t)ne * BLOCK * 128 * 2);
+            for (int e = 0; e < ne; ++e) {
+              const int krow = kvh * a.Sk + (int)(list[e0 + e] & 0xFFFFu) * BLOCK;
+              // d-halves are separate [128 rows][64] sub-tiles; block e fills rows e*BLOCK..
+              tma_load_2d_hint(dst + e * BLOCK * 128, map, &ctl->kv_full[stage], 0, krow, pol_kv);
+              tma_load_2d_hint(dst + kTileBytes / 2 + e * BLOCK * 128, map, &ctl->kv_full[stage],
+                               64, krow, pol_kv);
+            }
+          }
+          ++fills[stage];
+          ++L;
         }
-        ++fills[stage];
-        ++L;
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->list_empty[buf]);  // done reading this item's list
   }
   // drain: every copy this warp issued has landed before the CTA can exit
   for (int s = 0; s < kStages; ++s)
@@ -656,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->list_full[i], 1);
-      mbar_init(&ctl->list_empty[i], 9);  // the MMA thread + 8 softmax warps
+      mbar_init(&ctl->list_empty[i], 10);  // the TMA warp, the MMA thread, 8 softmax warps
       mbar_init(&ctl->q_full[i], 1);
       mbar_init(&ctl->q_empty[i], 2);     // one TMA-store leader per softmax warpgroup
       mbar_init(&ctl->p_full[i], 8);
@@ -700,6 +799,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_decrease<kOtherRegs>();
     if (warp == 8) {
       producer_role<BLOCK, JENGA>(smem, ctl, a, &tq, &tk, &tv);
+    } else if (warp == 10) {
+      list_role<BLOCK, JENGA>(smem, ctl, a);
     } else if (warp == 9) {
       if (lane_id() == 0) mma_role<BLOCK, JENGA>(smem, ctl, a, tmem);
       __syncwarp();
