@@ -33,7 +33,7 @@
 //   warps 0-3   softmax warpgroup 0: keys 0-63 of every key tile;
 //   warps 4-7   softmax warpgroup 1: keys 64-127 of every key tile.  One thread per
 //               query row; each warpgroup keeps its own running max m (log2 domain,
-//               allowed to lag the true max by up to 2^8 before O and l are rescaled),
+//               allowed to lag the true max by up to 2^32 before O and l are rescaled),
 //               row sums and O accumulator, so the two never synchronise inside the key
 //               loop.  After the item they merge (m, l, O) of both halves and each
 //               warpgroup normalises, stages and TMA-stores one 64-column half of the
@@ -56,7 +56,11 @@ constexpr int kThreads = 384;
 constexpr int kStages = 4;
 constexpr int kMaxNb = 2048;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per wait
-constexpr float kRescaleThreshold = 8.0f;         // log2 units: stale max allowed to lag 2^8
+// log2 units: the running max may lag the true one by up to 2^32 before O and l are
+// rescaled (each rescale waits for the previous PV).  P <= 2^32 is exact in range for
+// bf16; with at most 2048 * 64 keys per row, l <= 2^49 and |O| <= 2^49 max|v| stay
+// finite in fp32 for |v| < 6e23.
+constexpr float kRescaleThreshold = 32.0f;
 constexpr uint32_t kSoftmaxRegs = 216;            // per thread, softmax warpgroups
 constexpr uint32_t kOtherRegs = 56;               // per thread, TMA / MMA / list warps
 // registers the launch must provide for the re-balancing above (checked on the host)

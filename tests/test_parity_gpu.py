@@ -46,11 +46,26 @@ def test_random_ragged(block, seed):
 
 
 @pytest.mark.parametrize("block", [64, 128])
-def test_peaky_softmax_rescales(block):
-    # q, k x 4: the running max jumps by far more than the 2^8 lag allowed before a rescale
-    w = small(block, 11, max_kv=12, n_lo=6, qk_mul=4.0)
+@pytest.mark.parametrize("mul", [4.0, 8.0])
+def test_peaky_softmax_rescales(block, mul):
+    # q, k x 8: scores of std ~90 in log2 units, so the running max jumps by more than the
+    # 2^32 lag allowed before a rescale of O and l many times per row
+    w = small(block, 11, max_kv=12, n_lo=6, qk_mul=mul)
     out, lse = run_gpu(w)
     compare(w, out, lse)
+
+
+@pytest.mark.parametrize("block", [64, 128])
+def test_large_values_under_a_lagging_max(block):
+    # V x 2^10 (exact in bf16) on peaky scores: P up to 2^32 times V up to ~2^12 summed
+    # over 24 key blocks must stay finite, and out must be exactly 2^10 times the
+    # oracle's out for the unscaled V within the tolerance scaled by 2^10
+    w = small(block, 12, max_kv=24, n_lo=16, qk_mul=3.0)
+    dev = to_dev(w)
+    dev["v"] = dev["v"] * 1024.0
+    out, lse = run_gpu(w, dev)
+    assert bool(torch.isfinite(out.float()).all()) and bool(torch.isfinite(lse).all())
+    compare(w, (out.float() / 1024.0).to(torch.bfloat16), lse)
 
 
 @pytest.mark.parametrize("block", [64, 128])
