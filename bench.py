@@ -44,7 +44,7 @@ def attended_pairs(w) -> int:
     times the block's query rows."""
     if w.kind == "jenga":
         return int(w.bitmap.astype(bool).sum()) * w.block * w.block * w.B * w.H
-    nb = w.nb
+    nb = w.nbk
     vbs = np.clip(w.vbs.astype(np.int64), 0, w.block)
     n = np.clip(w.q2k_num.astype(np.int64), 0, w.max_kv)
     total = 0
@@ -149,11 +149,11 @@ def oracle_sample(w, budget_s: float, seed: int = 0):
     qb, kb, vb = workloads.bits(w.q), workloads.bits(w.k), workloads.bits(w.v)
     h = orc.load()
     threads = orc.num_threads(h)
-    allsel = orc.all_qblocks(w.B, w.H, w.nb)
+    allsel = orc.all_qblocks(w.B, w.H, w.nbq)
     rng = np.random.default_rng(seed)
     order = allsel[rng.permutation(len(allsel))]
     if w.kind == "vsa":
-        mask = orc.lut_to_blockmask(w.q2k_idx, w.q2k_num, w.nb, h=h)
+        mask = orc.lut_to_blockmask(w.q2k_idx, w.q2k_num, w.nbk, h=h)
     else:
         mask = w.bitmap
     vbs = w.vbs if w.kind == "vsa" else None
@@ -162,7 +162,7 @@ def oracle_sample(w, budget_s: float, seed: int = 0):
         tot = 0
         for (b, hh, q) in sel:
             row = mask[q] if mask.ndim == 2 else mask[b, hh, q]
-            vv = np.full(w.nb, w.block) if vbs is None else np.clip(vbs, 0, w.block)
+            vv = np.full(w.nbk, w.block) if vbs is None else np.clip(vbs, 0, w.block)
             tot += int(vv[row != 0].sum()) * w.block
         return tot
 
@@ -212,6 +212,10 @@ METRIC = "effective attended TFLOP/s (4*d*pairs) and % of GB300 bf16 TC peak"
 def config_of(w, pairs):
     c = {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "block": w.block,
          "attended_pairs": pairs, "l2": "flushed (256 MiB write) before every timed step"}
+    if w.Sk != w.S or w.Hkv != w.H:
+        c.update({"Hkv": w.Hkv, "Sk": w.Sk})
+    if w.extra.get("num_splits"):
+        c["num_splits"] = w.extra["num_splits"]
     if w.kind == "vsa":
         c["max_kv"] = w.max_kv
     else:
@@ -271,9 +275,19 @@ def main():
     lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
     wsbuf = binding.new_workspace(dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    split = w.kind == "vsa" and (w.Sk != w.S or w.Hkv != w.H)  # the split-KV route
+    if split:
+        n_split = binding.default_splits(w.B, w.H, w.S, w.block,
+                                         torch.cuda.get_device_properties(dev).multi_processor_count)
+        w.extra["num_splits"] = n_split
+        wsbuf = binding.new_split_workspace(w.B, w.H, w.S, w.block, n_split, dev)
 
     def step():
-        if w.kind == "vsa":
+        if split:
+            binding.vsa_fwd_split(q, k, v, idx, num, vbs, block=w.block, scale=w.scale,
+                                  num_splits=n_split, out=out, lse=lse, workspace=wsbuf,
+                                  stream=stream)
+        elif w.kind == "vsa":
             binding.vsa_fwd(q, k, v, idx, num, vbs, block=w.block, scale=w.scale, out=out,
                             lse=lse, workspace=wsbuf, stream=stream)
         else:
@@ -314,7 +328,35 @@ def main():
 
     # ---- end to end through the host-buffer entry point (VSA workloads)
     e2e = None
-    if w.kind == "vsa" and args.e2e_steps > 0:
+    if split and args.e2e_steps > 0:
+        # host buffers through the Python binding: copies in, split forward, copies out
+        h = dict(q=w.q.pin_memory(), k=w.k.pin_memory(), v=w.v.pin_memory(),
+                 idx=torch.from_numpy(w.q2k_idx).pin_memory(),
+                 num=torch.from_numpy(w.q2k_num).pin_memory(),
+                 vbs=torch.from_numpy(w.vbs).pin_memory())
+        d = dict(q=q, k=k, v=v, idx=idx, num=num, vbs=vbs)
+        h_out = torch.empty_like(w.q).pin_memory()
+        h_lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in h.values())
+        d2h = h_out.numel() * 2 + h_lse.numel() * 4
+
+        def e2e_step():
+            for key in d:
+                d[key].copy_(h[key], non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(2):
+            e2e_step()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e2e_ms = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps * 1e3, dist, dev)
+        e2e = {"value": ws * pairs * flop_per_pair / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    elif w.kind == "vsa" and args.e2e_steps > 0:
         h = dict(q=w.q.pin_memory(), k=w.k.pin_memory(), v=w.v.pin_memory(),
                  idx=torch.from_numpy(w.q2k_idx).pin_memory(),
                  num=torch.from_numpy(w.q2k_num).pin_memory(),
@@ -353,7 +395,7 @@ def main():
         p, t, nblk, threads = oracle_sample(w, 15.0)
         cpu = {"value": p * flop_per_pair / t / 1e12, "unit": "TFLOP/s", "cores": threads,
                "kind": "oracle",
-               "sample": f"{nblk} of {w.B * w.H * w.nb} query blocks of {w.name} "
+               "sample": f"{nblk} of {w.B * w.H * w.nbq} query blocks of {w.name} "
                          f"({p} attended pairs, {t:.1f} s)"}
 
     if rank == 0:

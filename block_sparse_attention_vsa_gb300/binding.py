@@ -6,7 +6,7 @@ CPU or eager-PyTorch fallback -- if the library is missing or was built for anot
 GPU the calls raise.
 
 Functions mirror the C entry points:
-  vsa_fwd, vsa_fwd_gqa, vsa_fwd_from_mask, jenga_fwd, vsa_lut_to_bitmap,
+  vsa_fwd, vsa_fwd_gqa, vsa_fwd_split, vsa_fwd_from_mask, jenga_fwd, vsa_lut_to_bitmap,
   vsa_bitmap_to_lut, vsa_fwd_from_host, vsa_device_status, vsa_workspace_bytes
 """
 from __future__ import annotations
@@ -29,7 +29,8 @@ MAX_BLOCKS = 2048
 EXPORTS = ("vsa_fwd", "jenga_fwd", "vsa_workspace_bytes", "vsa_lut_to_bitmap",
            "vsa_bitmap_to_lut", "vsa_fwd_from_host", "vsa_device_status",
            "vsa_last_launch_count", "vsa_status_str", "vsa_fwd_noalloc", "vsa_fwd_gqa",
-           "vsa_fwd_from_mask")
+           "vsa_fwd_from_mask", "vsa_fwd_split", "vsa_split_workspace_bytes")
+MAX_SPLITS = 64
 
 
 class VsaError(RuntimeError):
@@ -58,6 +59,11 @@ def load(path: str = LIB_PATH):
     h.vsa_fwd_gqa.restype = i32
     h.vsa_fwd_gqa.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32, P,
                               P, P, P]
+    h.vsa_fwd_split.restype = i32
+    h.vsa_fwd_split.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32,
+                                i32, P, P, P, sz, P]
+    h.vsa_split_workspace_bytes.restype = sz
+    h.vsa_split_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     h.vsa_fwd_from_mask.restype = i32
     h.vsa_fwd_from_mask.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32,
                                     P, P, P, P]
@@ -209,6 +215,58 @@ def vsa_fwd_gqa(q, k, v, q2k_idx, q2k_num, variable_block_sizes=None, block=64, 
                          Sq, Sk, D, idx.shape[-1], block, scale, _ptr(out), _ptr(lse_t),
                          _ptr(workspace), _stream(stream))
     _check("vsa_fwd_gqa", code)
+    return out, lse_t
+
+
+def split_workspace_bytes(B, Hq, Sq, block, num_splits) -> int:
+    return int(load().vsa_split_workspace_bytes(B, Hq, Sq, block, num_splits))
+
+
+def new_split_workspace(B, Hq, Sq, block, num_splits, device=None) -> torch.Tensor:
+    """Workspace for vsa_fwd_split: zeroed scheduling counters, then the partials."""
+    n = split_workspace_bytes(B, Hq, Sq, block, num_splits)
+    if n == 0:
+        raise ValueError("invalid split-KV shape")
+    return torch.zeros((n + 15) // 16 * 4, dtype=torch.int32, device=device or "cuda")
+
+
+def default_splits(B, Hq, Sq, block, sm_count) -> int:
+    """Ranges per item so that about one unit per SM exists (1 when the items already fill
+    the SMs).  Finer ranges measured slower: each range pays a Q load, a pipeline fill and
+    a 64 KB partial."""
+    nbq = Sq // block
+    items = B * Hq * ((nbq + 1) // 2 if block == 64 else nbq)
+    if items == 0 or items >= sm_count:
+        return 1
+    return max(1, min(MAX_SPLITS, -(-sm_count // items)))
+
+
+def vsa_fwd_split(q, k, v, q2k_idx, q2k_num, variable_block_sizes=None, block=64, scale=None,
+                  num_splits=None, out=None, lse=True, workspace=None, stream=None):
+    """Split-KV forward (shapes as vsa_fwd_gqa).  num_splits=None picks default_splits for
+    the current device; the workspace is allocated if not given."""
+    h = load()
+    B, Hq, Hkv, Sq, Sk, D = _qkv_gqa(q, k, v)
+    idx = _meta32(q2k_idx, "q2k_idx")
+    num = _meta32(q2k_num, "q2k_num")
+    nbq = Sq // block if block else 0
+    if idx.dim() != 4 or idx.shape[:3] != (B, Hq, nbq) or num.shape != (B, Hq, nbq):
+        raise ValueError("q2k_idx must be [B,Hq,Sq/block,max_kv] and q2k_num [B,Hq,Sq/block]")
+    vbs = None if variable_block_sizes is None else _meta32(variable_block_sizes,
+                                                             "variable_block_sizes")
+    if num_splits is None:
+        num_splits = default_splits(B, Hq, Sq, block,
+                                    torch.cuda.get_device_properties(q.device).multi_processor_count)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else _dev(out, "out", torch.bfloat16, 4)
+    lse_t = _lse_arg(lse, (B, Hq, Sq), q.device)
+    if workspace is None:
+        workspace = new_split_workspace(B, Hq, Sq, block, num_splits, q.device)
+    code = h.vsa_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(num), _ptr(vbs), B, Hq,
+                           Hkv, Sq, Sk, D, idx.shape[-1], block, scale, num_splits, _ptr(out),
+                           _ptr(lse_t), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                           _stream(stream))
+    _check("vsa_fwd_split", code)
     return out, lse_t
 
 

@@ -203,6 +203,8 @@ FwdArgs shape_args(const Shape& p, float* lse, void* workspace, unsigned int* st
   a.nbk = p.Sk / p.block;
   a.items_per_bh = p.block == 64 ? (a.nbq + 1) / 2 : a.nbq;
   a.n_items = (int)((long long)p.B * p.Hq * a.items_per_bh);
+  a.n_splits = 1;
+  a.part = nullptr;
   a.scale_log2 = p.scale * 1.4426950408889634f;
   return a;
 }
@@ -240,6 +242,15 @@ vsa_status launch_fwd(DeviceInfo* dev, int slot, const void* q, const void* k, c
   kern<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, args);
   if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
   t_last_launches = 1;
+  if (args.n_splits > 1) {
+    const int items = args.n_items / args.n_splits;
+    const long long rows = (long long)items * 128;
+    split_merge_kernel<BLOCK><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+        args.part, items, args.n_splits, args.items_per_bh, args.Sq,
+        static_cast<uint16_t*>(out), args.lse);
+    if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
+    t_last_launches = 2;
+  }
   return VSA_OK;
 }
 
@@ -250,6 +261,9 @@ unsigned int* status_word() {
   return status;
 }
 
+// the scheduling counters at the start of a workspace
+constexpr size_t kSchedBytes = 256;
+
 bool workspace_ok(const void* workspace) {
   return workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 3u) == 0;
 }
@@ -258,7 +272,8 @@ bool workspace_ok(const void* workspace) {
 vsa_status run_lut(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
                    const int32_t* q2k_idx, const int32_t* q2k_num, const int32_t* vbs,
                    const Shape& p, int max_kv, vsa_bf16* out, float* lse, void* workspace,
-                   vsa_stream_t stream, bool require_vbs) {
+                   vsa_stream_t stream, bool require_vbs, int n_splits = 1,
+                   size_t workspace_bytes = 0) {
   t_last_launches = 0;
   DeviceInfo* dev = nullptr;
   bool nothing = false;
@@ -274,6 +289,23 @@ vsa_status run_lut(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
   a.q2k_num = q2k_num;
   a.vbs = vbs;
   a.max_kv = max_kv;
+  if (n_splits > 1) {
+    // units (item, key-tile range); partials after the scheduling counters
+    const long long units = (long long)a.n_items * n_splits;
+    if (units > (long long)INT_MAX) return VSA_ERR_UNSUPPORTED;
+    const size_t need = kSchedBytes + (size_t)units * kPartFloats * sizeof(float);
+    if (workspace == nullptr || workspace_bytes < need ||
+        (reinterpret_cast<uintptr_t>(workspace) & 15u))
+      return VSA_ERR_INVALID_ARG;
+    const size_t qbytes = (size_t)p.rows_q() * p.D * 2;
+    if (overlaps(workspace, need, out, qbytes) || (lse && overlaps(workspace, need, lse,
+                                                                    (size_t)p.rows_q() * 4)) ||
+        overlaps(workspace, need, q, qbytes))
+      return VSA_ERR_INVALID_ARG;
+    a.n_splits = n_splits;
+    a.n_items = (int)units;
+    a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kSchedBytes);
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (p.block == 64) return launch_fwd<64, false>(dev, 0, q, k, v, out, p, a, s);
   return launch_fwd<128, false>(dev, 1, q, k, v, out, p, a, s);
@@ -308,7 +340,7 @@ vsa_status run_map(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
 
 extern "C" {
 
-size_t vsa_workspace_bytes(void) { return 256; }
+size_t vsa_workspace_bytes(void) { return kSchedBytes; }
 
 vsa_status vsa_fwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
                    const int32_t* q2k_idx, const int32_t* q2k_num,
@@ -328,6 +360,28 @@ vsa_status vsa_fwd_gqa(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
   const Shape p{B, Hq, Hkv, Sq, Sk, D, block, scale};
   return run_lut(q, k, v, q2k_idx, q2k_num, variable_block_sizes, p, max_kv, out, lse,
                  workspace, stream, false);
+}
+
+size_t vsa_split_workspace_bytes(int B, int Hq, int Sq, int block, int num_splits) {
+  if (B < 0 || Hq < 0 || Sq < 0 || (block != 64 && block != 128) || num_splits < 1 ||
+      Sq % block != 0)
+    return 0;
+  const long long nbq = Sq / block;
+  const long long items = (long long)B * Hq * (block == 64 ? (nbq + 1) / 2 : nbq);
+  return kSchedBytes + (size_t)(items * num_splits) * kPartFloats * sizeof(float);
+}
+
+vsa_status vsa_fwd_split(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
+                         const int32_t* q2k_idx, const int32_t* q2k_num,
+                         const int32_t* variable_block_sizes, int B, int Hq, int Hkv, int Sq,
+                         int Sk, int D, int max_kv, int block, float scale, int num_splits,
+                         vsa_bf16* out, float* lse, void* workspace, size_t workspace_bytes,
+                         vsa_stream_t stream) {
+  t_last_launches = 0;
+  if (num_splits < 1 || num_splits > VSA_MAX_SPLITS) return VSA_ERR_INVALID_ARG;
+  const Shape p{B, Hq, Hkv, Sq, Sk, D, block, scale};
+  return run_lut(q, k, v, q2k_idx, q2k_num, variable_block_sizes, p, max_kv, out, lse,
+                 workspace, stream, false, num_splits, workspace_bytes);
 }
 
 vsa_status jenga_fwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,

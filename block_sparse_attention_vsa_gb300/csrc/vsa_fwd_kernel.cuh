@@ -101,8 +101,9 @@ struct SmemCtl {
   uint64_t stats_bar[2];
   uint64_t epi_bar[2];
   uint64_t drain;
-  int hdr_item[2];
-  int hdr_n[2];  // list entries of the item
+  int hdr_item[2];  // work unit (item * n_splits + split), -1 = no more work
+  int hdr_n[2];     // list entries of the unit
+  int hdr_off[2];   // index of the unit's first entry in the item's list
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -121,9 +122,16 @@ struct FwdArgs {
   float* lse;              // [B*Hq*Sq] or null
   unsigned int* sched;     // null = static schedule; else {next item, CTAs done}
   unsigned int* status;    // device status word
+  float* part;             // split-KV partials [n_items][kPartFloats], or null
   int Hq, Hkv, group, Sq, Sk, nbq, nbk, max_kv, n_items, items_per_bh;
+  int n_splits;            // key-tile ranges per item; n_items counts units (item, range)
   float scale_log2;
 };
+
+// Split-KV partial of one unit: O [128 rows][128] fp32, unnormalised relative to the
+// row's m, then m, l_round, l_exact per row (m = -inf and l = 0 for a row that attended
+// nothing in the unit's range).
+constexpr int kPartFloats = 128 * 128 + 3 * 128;
 
 // Bounded wait on an mbarrier phase.  Gives up after kWaitLimitNs (recording `code` in
 // the device status word and raising the CTA's abort flag), or as soon as another role
@@ -192,10 +200,11 @@ __device__ ItemHead build_list(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, ui
     return h;
   }
   uint32_t* list = reinterpret_cast<uint32_t*>(smem + kOffList) + buf * kMaxNb;
-  int count = 0;
+  int count = 0, off = 0;
   if (h.item >= 0) {
-    h.bh = h.item / a.items_per_bh;
-    h.qa = (h.item - h.bh * a.items_per_bh) * C::kPairs;
+    const int item = h.item / a.n_splits;
+    h.bh = item / a.items_per_bh;
+    h.qa = (item - h.bh * a.items_per_bh) * C::kPairs;
     const bool pair = C::kPairs == 2 && h.qa + 1 < a.nbq;  // the second query block exists
     // the item's selection as byte maps (which start, and are always left, all zero)
     if (!JENGA) {
@@ -304,11 +313,22 @@ __device__ ItemHead build_list(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, ui
       count = nx + ny + cb;
     }
     __syncwarp();
+    if (a.n_splits > 1) {
+      // this unit's share of the item's key tiles: tiles [t0, t1) of n_t
+      const int split = h.item - item * a.n_splits;
+      const int n_t = (count + C::kSub - 1) / C::kSub;
+      const int t0 = (int)((long long)n_t * split / a.n_splits);
+      const int t1 = (int)((long long)n_t * (split + 1) / a.n_splits);
+      off = t0 * C::kSub;
+      const int end = t1 * C::kSub < count ? t1 * C::kSub : count;
+      count = end - off;
+    }
   }
   h.count = count;
   if (lane == 0) {
     ctl->hdr_item[buf] = h.item;
     ctl->hdr_n[buf] = count;
+    ctl->hdr_off[buf] = off;
     mbar_arrive(&ctl->list_full[buf]);
   }
   __syncwarp();
@@ -339,10 +359,12 @@ __device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
   for (uint32_t it = 0; ok; ++it) {
     const uint32_t buf = it & 1;
     if (!wait_bar(&ctl->list_full[buf], (it >> 1) & 1, ctl, a.status, 7)) break;
-    const int item = ctl->hdr_item[buf];
+    const int unit = ctl->hdr_item[buf];
     const int count = ctl->hdr_n[buf];
-    if (item < 0) break;
-    const uint32_t* list = reinterpret_cast<const uint32_t*>(smem + kOffList) + buf * kMaxNb;
+    if (unit < 0) break;
+    const uint32_t* list =
+        reinterpret_cast<const uint32_t*>(smem + kOffList) + buf * kMaxNb + ctl->hdr_off[buf];
+    const int item = unit / a.n_splits;
     const int bh = item / a.items_per_bh;
     const int qa = (item - bh * a.items_per_bh) * C::kPairs;
     // Q (also the item's output staging buffer): free once the item two back is stored
@@ -586,10 +608,12 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
   for (uint32_t it = 0;; ++it) {
     const uint32_t buf = it & 1;
     if (!wait_bar(&ctl->list_full[buf], (it >> 1) & 1, ctl, a.status, 20)) break;
-    const int item = ctl->hdr_item[buf];
+    const int unit = ctl->hdr_item[buf];
     const int count = ctl->hdr_n[buf];
-    if (item < 0) break;
-    const uint32_t* list = reinterpret_cast<const uint32_t*>(smem + kOffList) + buf * kMaxNb;
+    if (unit < 0) break;
+    const uint32_t* list =
+        reinterpret_cast<const uint32_t*>(smem + kOffList) + buf * kMaxNb + ctl->hdr_off[buf];
+    const int item = unit / a.n_splits;
     const int n_tiles = (count + C::kSub - 1) / C::kSub;
     float m_run = -INFINITY, l_exact = 0.0f, l_round = 0.0f;
     bool ok = true;
@@ -684,7 +708,10 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
     const float l_e = c[0] * le[0] + c[1] * le[1];
     const bool has = l_r > 0.0f;
     const float inv = has ? 1.0f / l_r : 0.0f;
-    const float f0 = c[0] * inv, f1 = c[1] * inv;
+    // split-KV units keep O unnormalised (relative to mm): the merge kernel divides
+    const bool split = a.part != nullptr;
+    float* part = split ? a.part + (size_t)unit * kPartFloats : nullptr;
+    const float f0 = split ? c[0] : c[0] * inv, f1 = split ? c[1] : c[1] * inv;
     // a half's O is read only if that half attended something in this item (the other
     // accumulator may still hold an earlier item's values)
     const bool use0 = __any_sync(0xffffffffu, lr[0] > 0.0f);
@@ -699,22 +726,26 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
       if (use0) tmem_ld_32x32b_x16(tO0 + col, o0);
       if (use1) tmem_ld_32x32b_x16(tO1 + col, o1);
       tmem_wait_ld();
+      float x[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        float v = 0.0f;
+        if (use0 && f0 != 0.0f) v = __uint_as_float(o0[k]) * f0;
+        if (use1 && f1 != 0.0f) v = fmaf(__uint_as_float(o1[k]), f1, v);
+        x[k] = v;
+      }
+      if (split) {
+        float4* dst = reinterpret_cast<float4*>(part + row * 128 + col);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dst[j] = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+        continue;
+      }
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         uint32_t wv[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float x[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int k = 8 * i + 2 * j + u;
-            float v = 0.0f;
-            if (use0 && f0 != 0.0f) v = __uint_as_float(o0[k]) * f0;
-            if (use1 && f1 != 0.0f) v = fmaf(__uint_as_float(o1[k]), f1, v);
-            x[u] = v;
-          }
-          wv[j] = pack_bf16x2(x[0], x[1]);
-        }
+        for (int j = 0; j < 4; ++j) wv[j] = pack_bf16x2(x[8 * i + 2 * j], x[8 * i + 2 * j + 1]);
         const uint32_t chunk = (uint32_t)(cc * 2 + i);      // 16-byte chunk in the 128B row
         const uint32_t phys = chunk ^ (uint32_t)(row & 7);  // 128-byte swizzle
         uint8_t* dst = qs + row * 128 + phys * 16;
@@ -723,8 +754,15 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
                      : "memory");
       }
     }
-    if (w == 0 && a.lse != nullptr && qa * BLOCK + row < a.Sq)
+    if (split) {
+      if (w == 0) {
+        part[128 * 128 + row] = has ? mm : -INFINITY;
+        part[128 * 128 + 128 + row] = l_r;
+        part[128 * 128 + 256 + row] = l_e;
+      }
+    } else if (w == 0 && a.lse != nullptr && qa * BLOCK + row < a.Sq) {
       a.lse[(long long)bh * a.Sq + qa * BLOCK + row] = has ? mm + log2f(l_e) : -3.402823466e+38f;
+    }
     tc_fence_before();
     fence_proxy_async_smem();
     __syncwarp();
@@ -736,9 +774,11 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
     if (n_tiles > 0) ++ne_items;
     if (leader) {
       if (!wait_bar(&ctl->epi_bar[w], it & 1, ctl, a.status, 24)) break;
-      tma_store_3d(to, qs, w * 64, qa * BLOCK, bh);  // rows past Sq are not written
-      bulk_commit_group();
-      bulk_wait_group_read0();
+      if (!split) {
+        tma_store_3d(to, qs, w * 64, qa * BLOCK, bh);  // rows past Sq are not written
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
       mbar_arrive(&ctl->q_empty[buf]);
     }
   }
@@ -824,6 +864,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       atomicExch(&a.sched[1], 0u);
     }
   }
+}
+
+// ------------------------------------------------------------------------------------
+// Split-KV merge: one warp per query row combines the row's n_splits partials exactly as
+// the forward merges its two key halves: M = max m_s, c_s = 2^(m_s - M) (0 for an empty
+// partial), out = sum c_s O_s / sum c_s l_round_s, lse = M + log2(sum c_s l_exact_s).
+// Partials of item i are units i * n_splits .. i * n_splits + n_splits - 1.
+template <int BLOCK>
+__global__ void __launch_bounds__(256) split_merge_kernel(const float* __restrict__ part,
+                                                          int n_items, int n_splits,
+                                                          int items_per_bh, int Sq,
+                                                          uint16_t* __restrict__ out,
+                                                          float* __restrict__ lse) {
+  using C = Cfg<BLOCK>;
+  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);  // item * 128 + row
+  if (r >= (long long)n_items * 128) return;
+  const int item = (int)(r >> 7), row = (int)(r & 127);
+  const int bh = item / items_per_bh;
+  const int qrow = (item - bh * items_per_bh) * C::kPairs * BLOCK + row;
+  if (qrow >= Sq) return;  // the rows past a lone last query block
+  const uint32_t lane = threadIdx.x & 31;
+  const float* p0 = part + (size_t)item * n_splits * kPartFloats;
+  float M = -INFINITY;
+  for (int s = 0; s < n_splits; ++s) {
+    const float* st = p0 + (size_t)s * kPartFloats + 128 * 128;
+    if (st[128 + row] > 0.0f) M = fmaxf(M, st[row]);
+  }
+  float lr = 0.0f, le = 0.0f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < n_splits; ++s) {
+    const float* ps = p0 + (size_t)s * kPartFloats;
+    const float l_r = ps[128 * 128 + 128 + row];
+    if (!(l_r > 0.0f)) continue;
+    const float c = exp2f(ps[128 * 128 + row] - M);
+    lr = fmaf(c, l_r, lr);
+    le = fmaf(c, ps[128 * 128 + 256 + row], le);
+    const float4 o = reinterpret_cast<const float4*>(ps + row * 128)[lane];
+    acc.x = fmaf(c, o.x, acc.x);
+    acc.y = fmaf(c, o.y, acc.y);
+    acc.z = fmaf(c, o.z, acc.z);
+    acc.w = fmaf(c, o.w, acc.w);
+  }
+  const bool has = lr > 0.0f;
+  const float inv = has ? 1.0f / lr : 0.0f;
+  const long long orow = (long long)bh * Sq + qrow;
+  uint2 packed;
+  packed.x = pack_bf16x2(has ? acc.x * inv : 0.0f, has ? acc.y * inv : 0.0f);
+  packed.y = pack_bf16x2(has ? acc.z * inv : 0.0f, has ? acc.w * inv : 0.0f);
+  reinterpret_cast<uint2*>(out + orow * 128)[lane] = packed;
+  if (lse != nullptr && lane == 0) lse[orow] = has ? M + log2f(le) : -3.402823466e+38f;
 }
 
 }  // namespace vsa

@@ -22,6 +22,10 @@ The five workloads:
   jenga           B1 H16 S24576, 64x64 blocks, one i8 bitmap [384, 384] shared by
                   every head: the band kb - qb in [-8, 7] plus 8 distinct random
                   blocks outside the band per row
+  vsa_decode      B1 H24, 128 queries (one block-64 pair per head) against 98304 keys
+                  (1536 blocks): each query block takes 128 distinct random key blocks;
+                  variable_block_sizes 64 except the last block, 32 (a short query
+                  over a long video context, run through the split-KV path)
   vsa_long_video  B1 H24 S98304 block 64 (1536 blocks) on a 16x16x6 block grid,
                   id = (x*16 + y)*6 + z; every q-block takes the 112 blocks nearest
                   to it (squared Euclidean distance, ties by id, itself included)
@@ -234,12 +238,22 @@ def make_vsa_long_video(seed=0, H=24) -> Workload:
                     q2k_idx=idx, q2k_num=num, vbs=vbs)
 
 
+def make_vsa_decode(seed=0) -> Workload:
+    B, H, Sq, Sk, D, block = 1, 24, 128, 98304, HEAD_DIM, 64
+    w = make_random_gqa(B, H, H, Sq, Sk, D, block, 128, seed, n_lo=128, n_hi=128)
+    w.vbs = np.full(Sk // block, block, dtype=np.int32)
+    w.vbs[-1] = 32
+    w.name = "vsa_decode"
+    return w
+
+
 MAKERS = {
     "vsa_tiny": make_vsa_tiny,
     "vsa_mid": make_vsa_mid,
     "vsa_blk128": make_vsa_blk128,
     "jenga": make_jenga,
     "vsa_long_video": make_vsa_long_video,
+    "vsa_decode": make_vsa_decode,
 }
 
 

@@ -68,6 +68,8 @@ typedef enum vsa_status {
 #define VSA_HEAD_DIM 128
 /* Largest number of key blocks per sequence (Sk / block) the kernels accept. */
 #define VSA_MAX_BLOCKS 2048
+/* Largest num_splits vsa_fwd_split accepts. */
+#define VSA_MAX_SPLITS 64
 
 /* every entry point is exported from the shared library */
 #if defined(__GNUC__)
@@ -156,6 +158,39 @@ VSA_API vsa_status vsa_fwd_from_mask(const vsa_bf16 *q, const vsa_bf16 *k, const
                                      int Hkv, int Sq, int Sk, int D, int block, float scale,
                                      vsa_bf16 *out, float *lse, void *workspace,
                                      vsa_stream_t stream);
+
+/* Split-KV forward: vsa_fwd_gqa with each work item's key tiles divided into num_splits
+ * contiguous ranges processed by different CTAs, then combined by a second kernel.  For
+ * shapes with few work items (a short query, few heads) and long key lists, where one
+ * CTA per item would leave most SMs idle.
+ *   A work item is 128 query rows (one block-128 query block, or an adjacent pair of
+ *   block-64 query blocks); its selected key blocks form key tiles of 128 keys, and range
+ *   s of n tiles is tiles [n*s/num_splits, n*(s+1)/num_splits) (possibly empty).
+ *   Each range leaves in the workspace an fp32 partial: O [128][128] relative to the
+ *   row's running maximum m, then m, the sum of the bf16-rounded weights and the sum of
+ *   the fp32 weights per row; the merge takes M = max m_s and c_s = 2^(m_s - M) and
+ *   writes out = sum c_s O_s / sum c_s l_round_s and lse = M + log2(sum c_s l_exact_s),
+ *   the same arithmetic the single-pass kernel uses to join its two key halves, so the
+ *   result matches vsa_fwd_gqa within rounding (not bit for bit).
+ *   num_splits   1..VSA_MAX_SPLITS; 1 is vsa_fwd_gqa (workspace then optional, as there).
+ *   workspace    device memory of at least vsa_split_workspace_bytes(B, Hq, Sq, block,
+ *                num_splits) bytes, 16-byte aligned, whose first vsa_workspace_bytes()
+ *                bytes are zero before the call (they are left zero); the rest needs no
+ *                initialisation.  Must not overlap q, out or lse.  Calls sharing a
+ *                workspace must not overlap on the GPU.
+ *   workspace_bytes  its size; a smaller one is VSA_ERR_INVALID_ARG.
+ *   Other arguments and errors as vsa_fwd_gqa.  Enqueues two kernels.
+ * Source: the split-K decode pattern of "vLLM FlyDSL tq_decode" (partial (m, l, O) per
+ * key partition plus a reduction); the arithmetic of each part is that of vsa_fwd. */
+VSA_API vsa_status vsa_fwd_split(const vsa_bf16 *q, const vsa_bf16 *k, const vsa_bf16 *v,
+                                 const int32_t *q2k_idx, const int32_t *q2k_num,
+                                 const int32_t *variable_block_sizes, int B, int Hq, int Hkv,
+                                 int Sq, int Sk, int D, int max_kv, int block, float scale,
+                                 int num_splits, vsa_bf16 *out, float *lse, void *workspace,
+                                 size_t workspace_bytes, vsa_stream_t stream);
+
+/* Workspace bytes vsa_fwd_split needs for this shape (0 for an invalid one). */
+VSA_API size_t vsa_split_workspace_bytes(int B, int Hq, int Sq, int block, int num_splits);
 
 /* Bytes of device workspace the forward entry points use when given one. */
 VSA_API size_t vsa_workspace_bytes(void);

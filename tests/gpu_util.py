@@ -30,10 +30,14 @@ def to_dev(w):
     return r
 
 
-def run_gpu(w, dev=None, lse=True, workspace=None):
+def run_gpu(w, dev=None, lse=True, workspace=None, splits=None):
     dev = dev or to_dev(w)
     gqa = w.Hkv != w.H or w.Sk != w.S
-    if w.kind == "vsa" and gqa:
+    if splits is not None:
+        out, l = binding.vsa_fwd_split(dev["q"], dev["k"], dev["v"], dev["idx"], dev["num"],
+                                       dev["vbs"], block=w.block, scale=w.scale,
+                                       num_splits=splits, lse=lse, workspace=workspace)
+    elif w.kind == "vsa" and gqa:
         out, l = binding.vsa_fwd_gqa(dev["q"], dev["k"], dev["v"], dev["idx"], dev["num"],
                                      dev["vbs"], block=w.block, scale=w.scale, lse=lse,
                                      workspace=workspace)
