@@ -14,6 +14,8 @@ the arithmetic is in vsa_oracle.c, which cites the passages it follows:
                      give +0.0 and LSE_EMPTY
   vsa_forward        lut_to_blockmask followed by masked_attention
   jenga_forward      masked_attention on the shared bitmap
+  masked_attention_bwd / vsa_backward
+                     the fp64 gradients dq, dk, dv of the same forward for a given dout
 """
 from __future__ import annotations
 
@@ -75,6 +77,9 @@ def load(lib: str = LIB, src: str = SRC):
     h.oracle_masked_attention.restype = None
     h.oracle_masked_attention.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P, i64,
                                           i64, i32, P, f64, P, i64, P, P]
+    h.oracle_masked_attention_bwd.restype = None
+    h.oracle_masked_attention_bwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, P,
+                                              i64, i64, i32, P, f64, P, P, P]
     if lib == LIB:
         _lib = h
     return h
@@ -176,6 +181,47 @@ def jenga_forward(q_bits, k_bits, v_bits, bitmap, block: int, scale: float, sel=
     """Jenga forward: i8 bitmap [nb,nb] shared by every (b,h); nonzero = attend."""
     return masked_attention(q_bits, k_bits, v_bits, bitmap, block, scale, vbs=None, sel=sel,
                             h=h)
+
+
+def masked_attention_bwd(q_bits, k_bits, v_bits, dout_bits, blockmask, block: int,
+                         scale: float, vbs=None, h=None):
+    """Oracle backward on bf16 bit patterns (shapes as masked_attention, dout like q).
+    Returns (dq [B,Hq,Sq,D], dk [B,Hkv,Sk,D], dv [B,Hkv,Sk,D]) in float64."""
+    h = h or load()
+    q = _c(q_bits, np.uint16)
+    k = _c(k_bits, np.uint16)
+    v = _c(v_bits, np.uint16)
+    do = _c(dout_bits, np.uint16)
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    assert v.shape == k.shape and do.shape == q.shape and Bk == B and Dk == D
+    assert Hq % Hkv == 0 and Sq % block == 0 and Sk % block == 0
+    nbq, nbk = Sq // block, Sk // block
+    m = _c(blockmask, np.int8)
+    if m.ndim == 2:
+        assert m.shape == (nbq, nbk)
+        sb, sh = 0, 0
+    else:
+        assert m.shape == (B, Hq, nbq, nbk)
+        sb, sh = Hq, 1
+    vb = None if vbs is None else _c(vbs, np.int32)
+    dq = np.empty((B, Hq, Sq, D), dtype=np.float64)
+    dk = np.empty((B, Hkv, Sk, D), dtype=np.float64)
+    dv = np.empty((B, Hkv, Sk, D), dtype=np.float64)
+    h.oracle_masked_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Hq, Hkv, Sq, Sk, D,
+                                  _ptr(m), sb, sh, block, None if vb is None else _ptr(vb),
+                                  float(scale), _ptr(dq), _ptr(dk), _ptr(dv))
+    return dq, dk, dv
+
+
+def vsa_backward(q_bits, k_bits, v_bits, dout_bits, q2k_idx, q2k_num, vbs, block: int,
+                 scale: float, h=None):
+    """VSA backward: LUT -> block mask -> masked_attention_bwd."""
+    h = h or load()
+    nbk = k_bits.shape[2] // block
+    mask = lut_to_blockmask(q2k_idx, q2k_num, nbk, h=h)
+    return masked_attention_bwd(q_bits, k_bits, v_bits, dout_bits, mask, block, scale, vbs=vbs,
+                                h=h)
 
 
 def scatter_rows(out_sel, lse_sel, sel, B, H, S, block):

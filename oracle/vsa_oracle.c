@@ -215,3 +215,109 @@ void oracle_masked_attention(const uint16_t *q, const uint16_t *k,
     free(acc);
   }
 }
+
+/* Backward of steps 2-4 (the gradient of the forward above with respect to q, k and v,
+ * given the gradient dout of out).  The pages name the backward only ("FastVideo
+ * block_sparse_attn_sm100a.py", module docstring: the Triton backward consumes the
+ * forward's lse); the definition is the textbook gradient of softmax attention,
+ * restricted to the attended keys A_i of row i:
+ *
+ *   s_ij  = scale * q_i . k_j,      p_ij = exp(s_ij - L_i)  (L_i = ln sum_j exp s_ij)
+ *   dp_ij = dout_i . v_j,           D_i  = sum_{j in A_i} p_ij dp_ij  (= dout_i . out_i)
+ *   ds_ij = p_ij (dp_ij - D_i)
+ *   dq_i  = scale * sum_j ds_ij k_j
+ *   dk_j  = scale * sum_i ds_ij q_i          (over every row i attending j, every
+ *   dv_j  =         sum_i p_ij dout_i         query head of j's key/value group)
+ *
+ * Rows with no attended key contribute nothing and get dq = 0.  Shapes as
+ * oracle_masked_attention; dout [B, Hq, Sq, D] bf16 bits; every (b, h, query block) is
+ * computed.  dq [B, Hq, Sq, D], dk and dv [B, Hkv, Sk, D], double, overwritten.
+ */
+void oracle_masked_attention_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                 const uint16_t *dout, int B, int Hq, int Hkv, int Sq,
+                                 int Sk, int D, const int8_t *blockmask,
+                                 int64_t mask_stride_b, int64_t mask_stride_h, int block,
+                                 const int32_t *vbs, double scale, double *dq, double *dk,
+                                 double *dv) {
+  const int nbq = Sq / block, nbk = Sk / block;
+  const int group = Hq / Hkv;
+  memset(dq, 0, sizeof(double) * (size_t)B * Hq * Sq * D);
+  memset(dk, 0, sizeof(double) * (size_t)B * Hkv * Sk * D);
+  memset(dv, 0, sizeof(double) * (size_t)B * Hkv * Sk * D);
+  /* parallel over key/value heads: each owns its dk, dv and its group's dq rows */
+#pragma omp parallel
+  {
+    double *s_buf = (double *)malloc(sizeof(double) * (size_t)Sk);
+    double *dp_buf = (double *)malloc(sizeof(double) * (size_t)Sk);
+    int32_t *j_buf = (int32_t *)malloc(sizeof(int32_t) * (size_t)Sk);
+    double *qrow = (double *)malloc(sizeof(double) * (size_t)D);
+    double *drow = (double *)malloc(sizeof(double) * (size_t)D);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t bkv = 0; bkv < (int64_t)B * Hkv; ++bkv) {
+      const int b = (int)(bkv / Hkv), hk = (int)(bkv % Hkv);
+      const uint16_t *kh = k + bkv * Sk * (int64_t)D;
+      const uint16_t *vh = v + bkv * Sk * (int64_t)D;
+      double *dkh = dk + bkv * Sk * (int64_t)D;
+      double *dvh = dv + bkv * Sk * (int64_t)D;
+      for (int h = hk * group; h < (hk + 1) * group; ++h) {
+        const int64_t bh = (int64_t)b * Hq + h;
+        const uint16_t *qh = q + bh * Sq * (int64_t)D;
+        const uint16_t *doh = dout + bh * Sq * (int64_t)D;
+        double *dqh = dq + bh * Sq * (int64_t)D;
+        for (int i = 0; i < Sq; ++i) {
+          const int qb = i / block;
+          const int8_t *mrow = blockmask +
+                               (b * mask_stride_b + h * mask_stride_h) *
+                                   (int64_t)nbq * nbk +
+                               (int64_t)qb * nbk;
+          for (int d = 0; d < D; ++d) {
+            qrow[d] = bf16_to_double(qh[(int64_t)i * D + d]);
+            drow[d] = bf16_to_double(doh[(int64_t)i * D + d]);
+          }
+          int64_t n_att = 0;
+          for (int j = 0; j < Sk; ++j) {
+            const int kb = j / block;
+            const int valid = vbs ? vbs[kb] : block;
+            if (mrow[kb] == 0 || (j % block) >= valid) continue;
+            double dot = 0.0, dpd = 0.0;
+            for (int d = 0; d < D; ++d) {
+              dot += qrow[d] * bf16_to_double(kh[(int64_t)j * D + d]);
+              dpd += drow[d] * bf16_to_double(vh[(int64_t)j * D + d]);
+            }
+            s_buf[n_att] = scale * dot;
+            dp_buf[n_att] = dpd;
+            j_buf[n_att] = j;
+            ++n_att;
+          }
+          if (n_att == 0) continue;
+          double m = s_buf[0];
+          for (int64_t a = 1; a < n_att; ++a)
+            if (s_buf[a] > m) m = s_buf[a];
+          double l = 0.0;
+          for (int64_t a = 0; a < n_att; ++a) l += exp(s_buf[a] - m);
+          double Di = 0.0;
+          for (int64_t a = 0; a < n_att; ++a) {
+            s_buf[a] = exp(s_buf[a] - m) / l; /* now p_ij */
+            Di += s_buf[a] * dp_buf[a];
+          }
+          for (int64_t a = 0; a < n_att; ++a) {
+            const double p = s_buf[a];
+            const double ds = p * (dp_buf[a] - Di);
+            const int64_t j = j_buf[a];
+            for (int d = 0; d < D; ++d) {
+              const double kd = bf16_to_double(kh[j * D + d]);
+              dqh[(int64_t)i * D + d] += scale * ds * kd;
+              dkh[j * D + d] += scale * ds * qrow[d];
+              dvh[j * D + d] += p * drow[d];
+            }
+          }
+        }
+      }
+    }
+    free(s_buf);
+    free(dp_buf);
+    free(j_buf);
+    free(qrow);
+    free(drow);
+  }
+}

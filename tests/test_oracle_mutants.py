@@ -2,7 +2,8 @@
 the pins in test_oracle_pins.py catch every one of them.
 
 Each mutant is the oracle's C source with one textual change: a dropped term, a wrong
-sign, a wrong index, a transposed operand, an off-by-one in a mask.  A mutant that no
+sign, a wrong index, a transposed operand, an off-by-one in a mask.  An anchor that
+occurs in both the forward and the backward gives one mutant per occurrence.  A mutant that no
 pin rejects would mean the pins leave that part of the oracle unchecked.
 """
 import os
@@ -36,19 +37,46 @@ MUTANTS = {
                        "for (int kb = nb - 1; kb >= 0; --kb) {\n      if (mrow[kb] != 0) {"),
     "bitmap_byte_must_be_one": ("if (mrow[kb] != 0) {", "if (mrow[kb] == 1) {"),
     "kv_head_interleaved": ("(int64_t)b * Hkv + h / group;", "(int64_t)b * Hkv + h % Hkv;"),
-    "kv_head_stride_query_length": ("k + bkv * Sk * (int64_t)D", "k + bkv * Sq * (int64_t)D"),
+    "kv_head_stride_query_length": (
+        "const uint16_t *kh = k + bkv * Sk * (int64_t)D;\n      const uint16_t *vh = v + bkv * Sk * (int64_t)D;\n      const int8_t",
+        "const uint16_t *kh = k + bkv * Sq * (int64_t)D;\n      const uint16_t *vh = v + bkv * Sk * (int64_t)D;\n      const int8_t"),
+    "bwd_kv_group_of_first_head": ("for (int h = hk * group; h < (hk + 1) * group; ++h) {",
+                                   "for (int h = hk; h < hk + 1; ++h) {"),
     "mask_row_stride_query_blocks": ("(int64_t)qb * nbk;", "(int64_t)qb * nbq;"),
+    "bwd_no_row_term": ("const double ds = p * (dp_buf[a] - Di);",
+                        "const double ds = p * dp_buf[a];"),
+    "bwd_dv_from_ds": ("dvh[j * D + d] += p * drow[d];", "dvh[j * D + d] += ds * drow[d];"),
+    "bwd_dq_scale_dropped": ("dqh[(int64_t)i * D + d] += scale * ds * kd;",
+                             "dqh[(int64_t)i * D + d] += ds * kd;"),
+    "bwd_dk_from_dout": ("dkh[j * D + d] += scale * ds * qrow[d];",
+                         "dkh[j * D + d] += scale * ds * drow[d];"),
+    "bwd_dp_from_k": ("dpd += drow[d] * bf16_to_double(vh[(int64_t)j * D + d]);",
+                      "dpd += drow[d] * bf16_to_double(kh[(int64_t)j * D + d]);"),
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_pins_reject_mutant(name):
+def _cases():
+    """One mutant per occurrence of each anchor: the forward and the backward repeat some
+    lines (the token mask, the score), and a slip in either copy must be caught."""
+    src = open(orc.SRC).read()
+    out = []
+    for name in sorted(MUTANTS):
+        n = src.count(MUTANTS[name][0])
+        assert n >= 1, "mutation anchor missing: " + name
+        out += [(name, i) for i in range(n)]
+    return out
+
+
+@pytest.mark.parametrize("name,occ", _cases(), ids=lambda x: str(x))
+def test_pins_reject_mutant(name, occ):
     src = open(orc.SRC).read()
     old, new = MUTANTS[name]
-    assert src.count(old) == 1, "mutation anchor must be unique: " + name
+    pos = -1
+    for _ in range(occ + 1):
+        pos = src.index(old, pos + 1)
     with tempfile.TemporaryDirectory() as d:
         msrc = os.path.join(d, "mutant.c")
-        open(msrc, "w").write(src.replace(old, new))
+        open(msrc, "w").write(src[:pos] + new + src[pos + len(old):])
         lib = orc.build(msrc, os.path.join(d, "libmutant.so"), openmp=False)
         h = orc.load(lib, msrc)
         caught = []
@@ -57,4 +85,4 @@ def test_pins_reject_mutant(name):
                 pin(h)
             except AssertionError:
                 caught.append(pin.__name__)
-        assert caught, "no pin rejects mutant " + name
+        assert caught, "no pin rejects mutant %s (occurrence %d)" % (name, occ)

@@ -17,6 +17,10 @@ mistake is caught.
   pin_empty         empty rows: +0.0 (sign bit clear) and the finite sentinel
   pin_encodings     LUT -> bitmap -> attention is bit-identical to LUT -> attention;
                     bitmap <-> LUT conversions against Python set arithmetic
+  pin_backward      dq, dk, dv equal fp64 torch autograd: of scaled_dot_product_attention
+                    on group-repeated K/V (dense, Sq != Sk), and of a masked softmax
+                    written with torch.where over a token mask built by scanning the LUT
+                    (tail masks, empty rows, per-head selections)
   pin_gqa_cross     grouped-query heads (Hq = 3 Hkv) and Sq != Sk: dense selection equals
                     fp64 scaled_dot_product_attention on K/V repeated per group; a tiny
                     per-head sparse case equals the brute-force enumeration on the
@@ -331,8 +335,71 @@ def pin_gqa_cross(h):
                 assert abs(lse[0, hq, i] - l) <= 1e-12
 
 
+def _token_mask(idx, num, vbs, B, H, Sq, Sk, block, max_kv):
+    """[B,H,Sq,Sk] bool by scanning each LUT row slot by slot (no block-mask array)."""
+    m = np.zeros((B, H, Sq, Sk), dtype=bool)
+    for b in range(B):
+        for hh in range(H):
+            for i in range(Sq):
+                qb = i // block
+                n = min(max(int(num[b, hh, qb]), 0), max_kv)
+                for s in range(n):
+                    kb = int(idx[b, hh, qb, s])
+                    if 0 <= kb < Sk // block:
+                        m[b, hh, i, kb * block:kb * block + int(vbs[kb])] = True
+    return m
+
+
+def pin_backward(h):
+    # dense: all blocks, full, grouped heads, Sq != Sk -> autograd of SDPA
+    B, Hq, Hkv, Sq, Sk, D, block = 1, 4, 2, 32, 48, 8, 8
+    q = _rand_bits((B, Hq, Sq, D), 901)
+    k, v = (_rand_bits((B, Hkv, Sk, D), 902 + i) for i in range(2))
+    do = _rand_bits((B, Hq, Sq, D), 905)
+    nbq, nbk = Sq // block, Sk // block
+    idx = np.broadcast_to(np.arange(nbk, dtype=np.int32), (B, Hq, nbq, nbk)).copy()
+    num = np.full((B, Hq, nbq), nbk, np.int32)
+    scale = 0.31
+    dq, dk, dv = orc.vsa_backward(q, k, v, do, idx, num, None, block, scale, h=h)
+    tq, tk, tv, tdo = (torch.from_numpy(_bits_to_f64(x)) for x in (q, k, v, do))
+    tq.requires_grad_(); tk.requires_grad_(); tv.requires_grad_()
+    g = Hq // Hkv
+    out = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk.repeat_interleave(g, dim=1), tv.repeat_interleave(g, dim=1), scale=scale)
+    out.backward(tdo)
+    for got, ref in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+        assert np.max(np.abs(got - ref.numpy())) <= 1e-11
+    # sparse: LUT with tail masks, an empty query block, per-head selections
+    rng = np.random.default_rng(13)
+    B, Hq, Hkv, Sq, Sk, D, block, max_kv = 1, 2, 1, 24, 40, 4, 8, 4
+    nbq, nbk = Sq // block, Sk // block
+    q = _rand_bits((B, Hq, Sq, D), 911, mul=1.5)
+    k, v = (_rand_bits((B, Hkv, Sk, D), 912 + i, mul=1.5) for i in range(2))
+    do = _rand_bits((B, Hq, Sq, D), 915)
+    idx = rng.integers(-1, nbk + 1, size=(B, Hq, nbq, max_kv)).astype(np.int32)
+    num = rng.integers(1, max_kv + 1, size=(B, Hq, nbq)).astype(np.int32)
+    num[0, 1, 2] = 0
+    vbs = rng.integers(0, block + 1, size=nbk).astype(np.int32)
+    vbs[0] = block
+    dq, dk, dv = orc.vsa_backward(q, k, v, do, idx, num, vbs, block, 0.43, h=h)
+    mask = torch.from_numpy(_token_mask(idx, num, vbs, B, Hq, Sq, Sk, block, max_kv))
+    tq, tk, tv, tdo = (torch.from_numpy(_bits_to_f64(x)) for x in (q, k, v, do))
+    tq.requires_grad_(); tk.requires_grad_(); tv.requires_grad_()
+    kr, vr = tk.repeat_interleave(Hq // Hkv, dim=1), tv.repeat_interleave(Hq // Hkv, dim=1)
+    s_ = 0.43 * tq @ kr.transpose(-1, -2)
+    mx = torch.where(mask, s_, torch.tensor(-math.inf, dtype=torch.float64)).amax(-1, keepdim=True)
+    mx = torch.where(torch.isinf(mx), torch.zeros_like(mx), mx).detach()
+    e = torch.where(mask, torch.exp(s_ - mx), torch.zeros_like(s_))
+    l_ = e.sum(-1, keepdim=True)
+    out = (e / torch.where(l_ > 0, l_, torch.ones_like(l_))) @ vr
+    out.backward(tdo)
+    for got, ref in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+        assert np.max(np.abs(got - ref.numpy())) <= 1e-11
+    assert np.all(dq[0, 1, 16:24] == 0.0)  # the empty query block
+
+
 PINS = [pin_golden, pin_dense, pin_bruteforce, pin_invariants, pin_closed_forms, pin_empty,
-        pin_encodings, pin_gqa_cross]
+        pin_encodings, pin_gqa_cross, pin_backward]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
