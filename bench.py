@@ -207,6 +207,7 @@ def run_reference(args, w, pairs_total, flop_per_pair):
 
 
 METRIC = "effective attended TFLOP/s (4*d*pairs) and % of GB300 bf16 TC peak"
+METRIC_BWD = "backward: effective attended TFLOP/s (10*d*pairs) and % of GB300 bf16 TC peak"
 
 
 def config_of(w, pairs):
@@ -232,6 +233,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"],
+                    help="bwd times vsa_bwd (dq, dk, dv) on the workload instead")
     args = ap.parse_args()
 
     import torch
@@ -240,7 +243,11 @@ def main():
     ws, rank, local = dist_env()
     w = workloads.make(args.workload, seed=0)
     pairs = attended_pairs(w)
-    flop_per_pair = 4 * w.D
+    bwd = args.pass_ == "bwd"
+    if bwd and w.kind != "vsa":
+        raise SystemExit("--pass bwd needs a LUT (vsa_*) workload")
+    # forward: QK^T and PV (2d each); backward: S recomputed, dP, dV, dK, dQ (2d each)
+    flop_per_pair = (10 if bwd else 4) * w.D
 
     if args.impl == "reference":
         if ws > 1:
@@ -282,8 +289,18 @@ def main():
         w.extra["num_splits"] = n_split
         wsbuf = binding.new_split_workspace(w.B, w.H, w.S, w.block, n_split, dev)
 
+    if bwd:
+        out, lse = binding.vsa_fwd_gqa(q, k, v, idx, num, vbs, block=w.block, scale=w.scale)
+        gen = torch.Generator().manual_seed(1)
+        dout = torch.randn(w.q.shape, generator=gen).to(torch.bfloat16).to(dev)
+        bws = torch.empty(binding.load().vsa_bwd_workspace_bytes(w.B, w.H, w.S, w.Sk, w.block),
+                          dtype=torch.uint8, device=dev)
+
     def step():
-        if split:
+        if bwd:
+            binding.vsa_bwd(q, k, v, out, dout, lse, idx, num, vbs, block=w.block,
+                            scale=w.scale, workspace=bws, stream=stream)
+        elif split:
             binding.vsa_fwd_split(q, k, v, idx, num, vbs, block=w.block, scale=w.scale,
                                   num_splits=n_split, out=out, lse=lse, workspace=wsbuf,
                                   stream=stream)
@@ -328,7 +345,9 @@ def main():
 
     # ---- end to end through the host-buffer entry point (VSA workloads)
     e2e = None
-    if split and args.e2e_steps > 0:
+    if bwd:
+        pass  # the host-buffer leg belongs to the forward line
+    elif split and args.e2e_steps > 0:
         # host buffers through the Python binding: copies in, split forward, copies out
         h = dict(q=w.q.pin_memory(), k=w.k.pin_memory(), v=w.v.pin_memory(),
                  idx=torch.from_numpy(w.q2k_idx).pin_memory(),
@@ -388,10 +407,13 @@ def main():
     achieved = pairs * flop_per_pair / (ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": TRAFFIC.get(w.name),
-                "peak_source": f"{peak_src} dense bf16 (burst)", "kernel": "bsa_fwd_kernel"}
+                "peak_source": f"{peak_src} dense bf16 (burst)",
+                "kernel": "bwd_kv_kernel" if bwd else "bsa_fwd_kernel"}
+    if bwd:
+        roofline["traffic"] = None
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not bwd:
         p, t, nblk, threads = oracle_sample(w, 15.0)
         cpu = {"value": p * flop_per_pair / t / 1e12, "unit": "TFLOP/s", "cores": threads,
                "kind": "oracle",
@@ -400,7 +422,8 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded, shapes of the workload)",

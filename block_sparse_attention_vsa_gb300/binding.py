@@ -6,7 +6,7 @@ CPU or eager-PyTorch fallback -- if the library is missing or was built for anot
 GPU the calls raise.
 
 Functions mirror the C entry points:
-  vsa_fwd, vsa_fwd_gqa, vsa_fwd_split, vsa_fwd_from_mask, jenga_fwd, vsa_lut_to_bitmap,
+  vsa_fwd, vsa_fwd_gqa, vsa_fwd_split, vsa_fwd_from_mask, jenga_fwd, vsa_bwd, vsa_lut_to_bitmap,
   vsa_bitmap_to_lut, vsa_fwd_from_host, vsa_device_status, vsa_workspace_bytes
 """
 from __future__ import annotations
@@ -29,7 +29,8 @@ MAX_BLOCKS = 2048
 EXPORTS = ("vsa_fwd", "jenga_fwd", "vsa_workspace_bytes", "vsa_lut_to_bitmap",
            "vsa_bitmap_to_lut", "vsa_fwd_from_host", "vsa_device_status",
            "vsa_last_launch_count", "vsa_status_str", "vsa_fwd_noalloc", "vsa_fwd_gqa",
-           "vsa_fwd_from_mask", "vsa_fwd_split", "vsa_split_workspace_bytes")
+           "vsa_fwd_from_mask", "vsa_fwd_split", "vsa_split_workspace_bytes", "vsa_bwd",
+           "vsa_bwd_workspace_bytes")
 MAX_SPLITS = 64
 
 
@@ -64,6 +65,11 @@ def load(path: str = LIB_PATH):
                                 i32, P, P, P, sz, P]
     h.vsa_split_workspace_bytes.restype = sz
     h.vsa_split_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    h.vsa_bwd.restype = i32
+    h.vsa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                          f32, P, P, P, P, sz, P]
+    h.vsa_bwd_workspace_bytes.restype = sz
+    h.vsa_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     h.vsa_fwd_from_mask.restype = i32
     h.vsa_fwd_from_mask.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32,
                                     P, P, P, P]
@@ -268,6 +274,34 @@ def vsa_fwd_split(q, k, v, q2k_idx, q2k_num, variable_block_sizes=None, block=64
                            _stream(stream))
     _check("vsa_fwd_split", code)
     return out, lse_t
+
+
+def vsa_bwd(q, k, v, out, dout, lse, q2k_idx, q2k_num, variable_block_sizes=None, block=64,
+            scale=None, workspace=None, stream=None):
+    """Backward of vsa_fwd_gqa: returns (dq, dk, dv) for upstream gradient dout, given the
+    forward's out and lse.  The workspace is allocated if not given."""
+    h = load()
+    B, Hq, Hkv, Sq, Sk, D = _qkv_gqa(q, k, v)
+    _dev(out, "out", torch.bfloat16, 4)
+    _dev(dout, "dout", torch.bfloat16, 4)
+    _dev(lse, "lse", torch.float32, 3)
+    idx = _meta32(q2k_idx, "q2k_idx")
+    num = _meta32(q2k_num, "q2k_num")
+    vbs = None if variable_block_sizes is None else _meta32(variable_block_sizes,
+                                                             "variable_block_sizes")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    if workspace is None:
+        n = int(h.vsa_bwd_workspace_bytes(B, Hq, Sq, Sk, block))
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    code = h.vsa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(idx),
+                     _ptr(num), _ptr(vbs), B, Hq, Hkv, Sq, Sk, D, idx.shape[-1], block, scale,
+                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                     workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("vsa_bwd", code)
+    return dq, dk, dv
 
 
 def vsa_fwd_from_mask(q, k, v, block_map, variable_block_sizes=None, block=64, scale=None,

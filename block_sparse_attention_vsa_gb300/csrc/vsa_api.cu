@@ -14,6 +14,7 @@
 
 #include "../../include/vsa.h"
 #include "vsa_fwd_kernel.cuh"
+#include "vsa_bwd_kernel.cuh"
 
 namespace vsa {
 
@@ -75,6 +76,7 @@ struct DeviceInfo {
   int major = 0, minor = 0;
   bool attr_set[4] = {false, false, false, false};
   int regs[4] = {0, 0, 0, 0};
+  bool bwd_attr_set[2] = {false, false};
 };
 std::mutex g_mu;
 DeviceInfo g_dev[64];
@@ -336,11 +338,145 @@ vsa_status run_map(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
   return launch_fwd<128, true>(dev, 3, q, k, v, out, p, a, s);
 }
 
+size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+// Backward workspace: the 0/1 block map, D per query row, the fp32 dQ accumulator.
+struct BwdLayout {
+  size_t bitmap, dvec, dq, total;
+};
+BwdLayout bwd_layout(long long B, long long Hq, long long Sq, long long Sk, int block) {
+  const long long nbq = Sq / block, nbk = Sk / block, rows = B * Hq * Sq;
+  BwdLayout l;
+  l.bitmap = 0;
+  l.dvec = align256((size_t)(B * Hq * nbq * nbk));
+  l.dq = l.dvec + align256((size_t)rows * 4);
+  l.total = l.dq + (size_t)rows * 128 * 4;
+  return l;
+}
+
+template <int BLOCK>
+vsa_status launch_bwd(DeviceInfo* dev, const BwdArgs& a, long long n_ctas, cudaStream_t s) {
+  using C = BwdCfg<BLOCK>;
+  auto kern = bwd_kv_kernel<BLOCK>;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!dev->bwd_attr_set[BLOCK == 128]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)C::kSmem) != cudaSuccess)
+        return VSA_ERR_CUDA;
+      dev->bwd_attr_set[BLOCK == 128] = true;
+    }
+  }
+  if (n_ctas > 0) kern<<<(unsigned)n_ctas, C::kThreads, C::kSmem, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
 
 size_t vsa_workspace_bytes(void) { return kSchedBytes; }
+
+size_t vsa_bwd_workspace_bytes(int B, int Hq, int Sq, int Sk, int block) {
+  if (B < 0 || Hq < 0 || Sq < 0 || Sk < 0 || (block != 64 && block != 128) ||
+      Sq % block != 0 || Sk % block != 0)
+    return 0;
+  return bwd_layout(B, Hq, Sq, Sk, block).total;
+}
+
+vsa_status vsa_bwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
+                   const vsa_bf16* out, const vsa_bf16* dout, const float* lse,
+                   const int32_t* q2k_idx, const int32_t* q2k_num,
+                   const int32_t* variable_block_sizes, int B, int Hq, int Hkv, int Sq, int Sk,
+                   int D, int max_kv, int block, float scale, vsa_bf16* dq, vsa_bf16* dk,
+                   vsa_bf16* dv, void* workspace, size_t workspace_bytes,
+                   vsa_stream_t stream) {
+  t_last_launches = 0;
+  const Shape p{B, Hq, Hkv, Sq, Sk, D, block, scale};
+  DeviceInfo* dev = nullptr;
+  bool nothing = false;
+  // the forward's checks on q, k, v and out (out is read here, never written)
+  vsa_status st = check_shape(q, k, v, out, lse, p, &dev, &nothing);
+  if (st != VSA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t kbytes = (size_t)p.rows_k() * 128 * 2, qbytes = (size_t)p.rows_q() * 128 * 2;
+  if (nothing) {  // no query rows: every key gets a zero gradient
+    if (p.rows_k() == 0) return VSA_OK;
+    if (!dk || !dv) return VSA_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(dk, 0, kbytes, s) != cudaSuccess ||
+        cudaMemsetAsync(dv, 0, kbytes, s) != cudaSuccess)
+      return VSA_ERR_CUDA;
+    return VSA_OK;
+  }
+  if (max_kv < 1 || !q2k_idx || !q2k_num || !dout || !lse || !dq) return VSA_ERR_INVALID_ARG;
+  if (p.rows_k() > 0 && (!dk || !dv)) return VSA_ERR_INVALID_ARG;
+  if (!aligned16(dout) || !aligned16(dq) || (p.rows_k() > 0 && (!aligned16(dk) || !aligned16(dv))))
+    return VSA_ERR_INVALID_ARG;
+  const BwdLayout lay = bwd_layout(B, Hq, Sq, Sk, block);
+  if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return VSA_ERR_INVALID_ARG;
+  // outputs must not overlap any input or one another
+  const void* ins[6] = {q, k, v, out, dout, lse};
+  const size_t insz[6] = {qbytes, kbytes, kbytes, qbytes, qbytes, (size_t)p.rows_q() * 4};
+  const void* outs[4] = {dq, dk, dv, workspace};
+  const size_t outsz[4] = {qbytes, kbytes, kbytes, lay.total};
+  for (int o = 0; o < 4; ++o) {
+    for (int i = 0; i < 6; ++i)
+      if (outsz[o] && insz[i] && outs[o] && ins[i] && overlaps(outs[o], outsz[o], ins[i], insz[i]))
+        return VSA_ERR_INVALID_ARG;
+    for (int o2 = o + 1; o2 < 4; ++o2)
+      if (outsz[o] && outsz[o2] && outs[o] && outs[o2] &&
+          overlaps(outs[o], outsz[o], outs[o2], outsz[o2]))
+        return VSA_ERR_INVALID_ARG;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int8_t* bitmap = reinterpret_cast<int8_t*>(ws + lay.bitmap);
+  float* Dv = reinterpret_cast<float*>(ws + lay.dvec);
+  float* dq_acc = reinterpret_cast<float*>(ws + lay.dq);
+  const int nbq = Sq / block, nbk = Sk / block;
+  const long long lut_rows = (long long)B * Hq * nbq, rows = p.rows_q();
+  int launches = 0;
+  if (nbk > 0) {
+    lut_to_bitmap_kernel<<<(unsigned)lut_rows, 128, 0, s>>>(q2k_idx, q2k_num, max_kv, nbk,
+                                                            bitmap);
+    ++launches;
+  }
+  bwd_prep_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(out, dout, rows, Dv);
+  ++launches;
+  if (cudaGetLastError() != cudaSuccess ||
+      cudaMemsetAsync(dq_acc, 0, (size_t)rows * 128 * 4, s) != cudaSuccess)
+    return VSA_ERR_CUDA;
+  BwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.dout = dout;
+  a.lse = lse;
+  a.Dv = Dv;
+  a.bitmap = bitmap;
+  a.vbs = variable_block_sizes;
+  a.dq_acc = dq_acc;
+  a.dk = dk;
+  a.dv = dv;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.group = Hq / Hkv;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.nbq = nbq;
+  a.nbk = nbk;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const long long n_ctas = (long long)B * Hkv * nbk;
+  st = block == 64 ? launch_bwd<64>(dev, a, n_ctas, s) : launch_bwd<128>(dev, a, n_ctas, s);
+  if (st != VSA_OK) return st;
+  if (n_ctas > 0) ++launches;
+  const long long n8 = rows * 16;
+  bwd_dq_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, s>>>(dq_acc, n8, dq);
+  if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
+  t_last_launches = launches + 1;
+  return VSA_OK;
+}
 
 vsa_status vsa_fwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
                    const int32_t* q2k_idx, const int32_t* q2k_num,

@@ -192,6 +192,36 @@ VSA_API vsa_status vsa_fwd_split(const vsa_bf16 *q, const vsa_bf16 *k, const vsa
 /* Workspace bytes vsa_fwd_split needs for this shape (0 for an invalid one). */
 VSA_API size_t vsa_split_workspace_bytes(int B, int Hq, int Sq, int block, int num_splits);
 
+/* Backward: dq, dk, dv of the vsa_fwd_gqa forward for an upstream gradient dout.
+ *   With p_ij = 2^(scale * log2(e) * q_i . k_j - lse_i) over the attended keys (0 for the
+ *   rest), D_i = dout_i . out_i and ds_ij = p_ij (dout_i . v_j - D_i):
+ *     dq_i = scale sum_j ds_ij k_j,  dk_j = scale sum_i ds_ij q_i,  dv_j = sum_i p_ij dout_i,
+ *   dk and dv summed over every query head of a key/value group.  Rows with no attended
+ *   key contribute nothing (their dq is 0); keys no row attends get dk = dv = 0.
+ *   q, k, v, q2k_idx, q2k_num, variable_block_sizes, shapes, max_kv, block, scale: as given
+ *     to the forward.
+ *   out          the forward's output [B, Hq, Sq, D] bf16.
+ *   lse          the forward's lse [B, Hq, Sq] fp32 (required).
+ *   dout         [B, Hq, Sq, D] bf16.
+ *   dq           [B, Hq, Sq, D] bf16 output;  dk, dv  [B, Hkv, Sk, D] bf16 outputs.
+ *   workspace    at least vsa_bwd_workspace_bytes(B, Hq, Sq, Sk, block) bytes, 256-byte
+ *                aligned, no initialisation needed (the block map, D and an fp32 dq
+ *                accumulator live there).
+ *   No output may overlap an input or another output.  Enqueues up to four kernels and
+ *   one memset; errors as vsa_fwd_gqa.
+ * Source: "FastVideo block_sparse_attn_sm100a.py", module docstring (the backward
+ * consumes the forward's base-2 lse); the gradient is that of softmax attention. */
+VSA_API vsa_status vsa_bwd(const vsa_bf16 *q, const vsa_bf16 *k, const vsa_bf16 *v,
+                           const vsa_bf16 *out, const vsa_bf16 *dout, const float *lse,
+                           const int32_t *q2k_idx, const int32_t *q2k_num,
+                           const int32_t *variable_block_sizes, int B, int Hq, int Hkv, int Sq,
+                           int Sk, int D, int max_kv, int block, float scale, vsa_bf16 *dq,
+                           vsa_bf16 *dk, vsa_bf16 *dv, void *workspace, size_t workspace_bytes,
+                           vsa_stream_t stream);
+
+/* Workspace bytes vsa_bwd needs for this shape (0 for an invalid one). */
+VSA_API size_t vsa_bwd_workspace_bytes(int B, int Hq, int Sq, int Sk, int block);
+
 /* Bytes of device workspace the forward entry points use when given one. */
 VSA_API size_t vsa_workspace_bytes(void);
 
