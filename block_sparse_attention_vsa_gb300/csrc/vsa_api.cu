@@ -410,7 +410,8 @@ vsa_status vsa_bwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
   }
   if (max_kv < 1 || !q2k_idx || !q2k_num || !dout || !lse || !dq) return VSA_ERR_INVALID_ARG;
   if (p.rows_k() > 0 && (!dk || !dv)) return VSA_ERR_INVALID_ARG;
-  if (!aligned16(dout) || !aligned16(dq) || (p.rows_k() > 0 && (!aligned16(dk) || !aligned16(dv))))
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(lse) ||
+      (p.rows_k() > 0 && (!aligned16(dk) || !aligned16(dv))))
     return VSA_ERR_INVALID_ARG;
   const BwdLayout lay = bwd_layout(B, Hq, Sq, Sk, block);
   if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))

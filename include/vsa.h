@@ -201,7 +201,7 @@ VSA_API size_t vsa_split_workspace_bytes(int B, int Hq, int Sq, int block, int n
  *   q, k, v, q2k_idx, q2k_num, variable_block_sizes, shapes, max_kv, block, scale: as given
  *     to the forward.
  *   out          the forward's output [B, Hq, Sq, D] bf16.
- *   lse          the forward's lse [B, Hq, Sq] fp32 (required).
+ *   lse          the forward's lse [B, Hq, Sq] fp32 (required, 16-byte aligned).
  *   dout         [B, Hq, Sq, D] bf16.
  *   dq           [B, Hq, Sq, D] bf16 output;  dk, dv  [B, Hkv, Sk, D] bf16 outputs.
  *   workspace    at least vsa_bwd_workspace_bytes(B, Hq, Sq, Sk, block) bytes, 256-byte
