@@ -128,6 +128,50 @@ def test_gqa_and_mask_empty_problems(lib):
     assert code == binding.VSA_ERR_UNSUPPORTED
 
 
+def _split(lib, splits=3, ws=8 << 20, ws_bytes=1 << 30, **kw):
+    P = ctypes.c_void_p
+    args = dict(B=1, Hq=2, Hkv=2, Sq=256, Sk=512, D=128, block=64)
+    args.update(kw)
+    return lib.vsa_fwd_split(P(1 << 20), P(2 << 20), P(3 << 20), P(4 << 20), P(5 << 20), None,
+                             args["B"], args["Hq"], args["Hkv"], args["Sq"], args["Sk"],
+                             args["D"], 4, args["block"], 0.088, splits, P(7 << 20), None,
+                             P(ws) if ws else None, ws_bytes, None)
+
+
+def test_split_validation(lib):
+    assert _split(lib, splits=0) == binding.VSA_ERR_INVALID_ARG
+    assert _split(lib, splits=binding.MAX_SPLITS + 1) == binding.VSA_ERR_INVALID_ARG
+    assert _split(lib, D=64) == binding.VSA_ERR_UNSUPPORTED
+    assert _split(lib, Sq=0) == binding.VSA_OK
+    # 2 heads x 2 query blocks of 128 rows x 3 ranges, plus the scheduling counters
+    n = lib.vsa_split_workspace_bytes(1, 2, 256, 64, 3)
+    assert n == 256 + 2 * 2 * 3 * (128 * 128 + 3 * 128) * 4
+    assert lib.vsa_split_workspace_bytes(1, 2, 100, 64, 3) == 0
+    assert lib.vsa_split_workspace_bytes(1, 2, 256, 64, 0) == 0
+
+
+def _bwd(lib, ws_bytes=1 << 30, **kw):
+    P = ctypes.c_void_p
+    args = dict(B=1, Hq=2, Hkv=1, Sq=256, Sk=512, D=128, block=64, max_kv=4)
+    args.update(kw)
+    return lib.vsa_bwd(P(1 << 20), P(2 << 20), P(3 << 20), P(4 << 20), P(5 << 20), P(6 << 20),
+                       P(7 << 20), P(8 << 20), None, args["B"], args["Hq"], args["Hkv"],
+                       args["Sq"], args["Sk"], args["D"], args["max_kv"], args["block"], 0.088,
+                       P(9 << 20), P(10 << 20), P(11 << 20), P(12 << 20), ws_bytes, None)
+
+
+def test_bwd_validation(lib):
+    assert _bwd(lib, D=64) == binding.VSA_ERR_UNSUPPORTED
+    assert _bwd(lib, block=32) == binding.VSA_ERR_UNSUPPORTED
+    assert _bwd(lib, Hkv=3) == binding.VSA_ERR_INVALID_ARG
+    assert _bwd(lib, Sk=100) == binding.VSA_ERR_INVALID_ARG
+    assert _bwd(lib, B=0) == binding.VSA_OK
+    # block map B*Hq*nbq*nbk bytes, D per row, fp32 dq accumulator (each 256-aligned)
+    n = lib.vsa_bwd_workspace_bytes(1, 2, 256, 512, 64)
+    assert n == 256 + 2 * 256 * 4 + 2 * 256 * 128 * 4
+    assert lib.vsa_bwd_workspace_bytes(1, 2, 256, 500, 64) == 0
+
+
 def test_metadata_validation(lib):
     P = ctypes.c_void_p
     assert lib.vsa_lut_to_bitmap(P(1 << 20), P(2 << 20), -1, 4, 8, P(3 << 20), None) == \
