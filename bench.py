@@ -440,7 +440,7 @@ def main():
 # DRAM bytes (read + write) per launch of the forward kernel from an ncu capture of the
 # same kernel build (profiles/bsa_fwd_kernel_<workload>.md); absent = not measured for
 # the current kernel.
-TRAFFIC = {"vsa_mid": 183.0e6, "vsa_blk128": 1611.1e6}
+TRAFFIC = {"vsa_mid": 182.9e6, "vsa_blk128": 1611.2e6}
 
 
 if __name__ == "__main__":
