@@ -136,3 +136,17 @@ def test_large_gqa_sampled():
     out, lse = run_gpu(w, workspace=binding.new_workspace())
     sel = sample_qblocks(w.B, w.H, w.nbq, 8, seed=1, must=(1,))
     compare(w, out, lse, sel)
+
+
+# --------------------------------------------------- the largest key-block count accepted
+@pytest.mark.parametrize("route", ["lut", "mask", "split"])
+def test_max_key_blocks_every_block_selected(route):
+    # 2048 key blocks of 64 keys (VSA_MAX_BLOCKS), every one selected by every query block:
+    # the longest list the kernel builds, a dense row of 131,072 keys
+    nbk = binding.MAX_BLOCKS
+    w = workloads.make_random_gqa(1, 2, 1, 128, nbk * 64, 128, 64, nbk, seed=150, n_lo=nbk,
+                                  kind="mask" if route == "mask" else "vsa", vbs_lo=60,
+                                  vbs_hi=64)
+    assert int(w.q2k_num.min()) == nbk
+    out, lse = run_gpu(w, splits=8 if route == "split" else None)
+    compare(w, out, lse)
