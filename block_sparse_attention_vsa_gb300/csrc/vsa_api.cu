@@ -1,7 +1,7 @@
 // vsa_api.cu -- the C ABI of libvsa_gb300.so (declared in include/vsa.h): host-side
-// argument checks, TMA tensor-map encoding, persistent-grid launch of the forward
-// kernel, the metadata conversion kernels, the host-buffer wrapper and the device
-// status word.
+// argument checks, TMA tensor-map encoding, persistent-grid launches of the forward
+// (LUT, block-map, grouped-query, cross-length and split-KV routes) and of the backward,
+// the metadata conversion kernels, the host-buffer wrapper and the device status word.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>

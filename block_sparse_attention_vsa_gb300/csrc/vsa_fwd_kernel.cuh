@@ -168,7 +168,7 @@ struct Cfg {
 };
 
 // ------------------------------------------------------------------------------------
-// producer warp: work items, block lists, TMA copies
+// list warp (work items, block lists) and TMA warp (copies)
 // ------------------------------------------------------------------------------------
 struct ItemHead {
   int item, count, bh, qa;
@@ -345,9 +345,8 @@ __device__ void list_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a) {
 
 // TMA warp: Q and the selected K/V tiles of each item, in the order the MMA consumes them.
 template <int BLOCK, bool JENGA>
-__device__ void producer_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a,
-                              const CUtensorMap* tq, const CUtensorMap* tk,
-                              const CUtensorMap* tv) {
+__device__ void tma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, const CUtensorMap* tq,
+                         const CUtensorMap* tk, const CUtensorMap* tv) {
   using C = Cfg<BLOCK>;
   const uint32_t lane = lane_id();
   const uint64_t pol_kv = policy_evict_last();
@@ -842,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     regs_decrease<kOtherRegs>();
     if (warp == 8) {
-      producer_role<BLOCK, JENGA>(smem, ctl, a, &tq, &tk, &tv);
+      tma_role<BLOCK, JENGA>(smem, ctl, a, &tq, &tk, &tv);
     } else if (warp == 10) {
       list_role<BLOCK, JENGA>(smem, ctl, a);
     } else if (warp == 9) {
