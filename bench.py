@@ -179,6 +179,39 @@ def oracle_sample(w, budget_s: float, seed: int = 0):
     return pairs, spent, used, threads
 
 
+def oracle_bwd_sample(w, budget_s: float):
+    """Time the oracle backward on the first query blocks of head 0 (all of its keys),
+    doubling the slice until about ``budget_s`` seconds; returns (pairs, seconds,
+    n_blocks, threads)."""
+    import torch
+    from oracle import oracle as orc
+    from block_sparse_attention_vsa_gb300 import workloads
+    h = orc.load()
+    threads = orc.num_threads(h)
+    hk = 0
+    kb = workloads.bits(w.k[:1, hk:hk + 1])
+    vb = workloads.bits(w.v[:1, hk:hk + 1])
+    g = torch.Generator().manual_seed(1)
+    n, spent, pairs, used = 1, 0.0, 0, 0
+    while n <= w.nbq:
+        rows = n * w.block
+        qb = workloads.bits(w.q[:1, :1, :rows])
+        dob = workloads.bits(torch.randn((1, 1, rows, w.D), generator=g).to(torch.bfloat16))
+        idx = np.ascontiguousarray(w.q2k_idx[:1, :1, :n])
+        num = np.ascontiguousarray(w.q2k_num[:1, :1, :n])
+        t0 = time.perf_counter()
+        orc.vsa_backward(qb, kb, vb, dob, idx, num, w.vbs, w.block, w.scale, h=h)
+        spent = time.perf_counter() - t0
+        mask = orc.lut_to_blockmask(idx, num, w.nbk, h=h)[0, 0]
+        vv = np.clip(w.vbs, 0, w.block)
+        pairs = int(sum(int(vv[r != 0].sum()) for r in mask)) * w.block
+        used = n
+        if spent >= budget_s / 2 or n == w.nbq:
+            break
+        n = min(w.nbq, n * 2)
+    return pairs, spent, used, threads
+
+
 def run_reference(args, w, pairs_total, flop_per_pair):
     """The oracle on the host cores: each step is a bounded sample of the workload."""
     ws, rank, _ = dist_env()
@@ -413,6 +446,12 @@ def main():
         roofline["traffic"] = None
 
     cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and bwd:
+        p, t, nblk, threads = oracle_bwd_sample(w, 15.0)
+        cpu = {"value": p * flop_per_pair / t / 1e12, "unit": "TFLOP/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"backward of query blocks 0..{nblk - 1} of head 0 of {w.name} "
+                         f"against all its keys ({p} attended pairs, {t:.1f} s)"}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not bwd:
         p, t, nblk, threads = oracle_sample(w, 15.0)
         cpu = {"value": p * flop_per_pair / t / 1e12, "unit": "TFLOP/s", "cores": threads,
