@@ -15,19 +15,19 @@
 //                     stay in SMEM; dK and dV accumulate in tensor-core fragments while the
 //                     CTA walks every (query head of the group, query block) that selects
 //                     the key block (a column of the 0/1 block map, compacted into an SMEM
-//                     list), 64 (block 64) or 32 (block 128) query rows a step, the next
-//                     step's rows copied in asynchronously while the current one computes:
-//                     S = Q K^T and dP = dO V^T (tensor cores), P and dS element-wise in
-//                     SMEM, then dV += P^T dO, dK += dS^T Q and dQ_part = dS K, the last
-//                     added to an fp32 dQ accumulator with atomics (several key blocks feed
-//                     every query row).
+//                     list), 32 query rows a step, the next step's rows copied in
+//                     asynchronously while the current one computes.  Each warp owns 16
+//                     keys: S^T = K Q^T and dP^T = V dO^T land in its registers, P^T and
+//                     dS^T are formed there and reused as the A operands of dV += P^T dO
+//                     and dK += dS^T Q (dK, dV stay in registers); dS^T goes through SMEM
+//                     for dQ_part = dS K, added to an fp32 dQ accumulator with vector
+//                     reductions (several key blocks feed every query row).
 //   bwd_dq_kernel     fp32 dQ accumulator -> bf16 dq.
-// The contractions use the warp-level bf16 tensor-core path (16x16x16 fragments, fp32
-// accumulation).
+// The contractions use the warp-level bf16 tensor-core path (mma.sync m16n8k16, fp32
+// accumulation, operands through ldmatrix).
 #pragma once
 
 #include <cuda_bf16.h>
-#include <mma.h>
 
 #include <cstdint>
 
@@ -90,37 +90,24 @@ struct BwdArgs {
 
 template <int BLOCK>
 struct BwdCfg {
-  static constexpr int kWarps = 16;
+  static constexpr int kWarps = BLOCK / 16;          // one warp per 16 keys: 4 or 8
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kMq = BLOCK == 128 ? 32 : 64;  // query rows per step
+  static constexpr int kMq = 32;                     // query rows per step
   static constexpr int kLdH = 128 + 8;               // bf16 row pitch of K, V, Q, dO tiles
-  static constexpr int kLdP = BLOCK + 8;             // bf16 row pitch of P, dS
-  static constexpr int kLdS = BLOCK + 4;             // fp32 row pitch of S, dP
-  static constexpr int kLdO = 128 + 4;               // fp32 row pitch of dQ / dK / dV staging
+  static constexpr int kLdT = kMq + 8;               // bf16 row pitch of the dS^T tile
   static constexpr int kMaxSteps = 2048;             // (query head, query block) list chunk
   static constexpr size_t kQBytes = (size_t)kMq * kLdH * 2;
   static constexpr size_t kOffK = 0;
   static constexpr size_t kOffV = kOffK + (size_t)BLOCK * kLdH * 2;
   static constexpr size_t kOffQ = kOffV + (size_t)BLOCK * kLdH * 2;   // Q[2]
   static constexpr size_t kOffDO = kOffQ + 2 * kQBytes;                // dO[2]
-  static constexpr size_t kOffF = kOffDO + 2 * kQBytes;               // S | dP, fp32
-  static constexpr size_t kFBytesSd = (size_t)2 * kMq * kLdS * 4;
-  static constexpr size_t kFBytesO = (size_t)(BLOCK > kMq ? BLOCK : kMq) * kLdO * 4;
-  static constexpr size_t kFBytes = kFBytesSd > kFBytesO ? kFBytesSd : kFBytesO;
-  static constexpr size_t kOffP = kOffF + kFBytes;
-  static constexpr size_t kOffDS = kOffP + (size_t)kMq * kLdP * 2;
-  static constexpr size_t kOffRow = kOffDS + (size_t)kMq * kLdP * 2;  // [2] x (lse, D)[kMq]
+  static constexpr size_t kOffDS = kOffDO + 2 * kQBytes;               // dS^T [BLOCK][kLdT]
+  static constexpr size_t kOffRow = kOffDS + (size_t)BLOCK * kLdT * 2; // [2] x (lse, D)[kMq]
   static constexpr size_t kOffList = kOffRow + 2 * 2 * kMq * 4;
   static constexpr size_t kSmem = kOffList + (size_t)kMaxSteps * 4 + 16;
-  static constexpr int kTilesKV = (BLOCK / 16) * 8;                  // dK or dV 16x16 tiles
-  static constexpr int kAccPerWarp = kTilesKV / kWarps;              // 2 or 4
-  static constexpr int kTilesQ = (kMq / 16) * 8;                     // dQ part tiles
-  static constexpr int kQPerWarp = kTilesQ / kWarps;                 // 2 or 1
-  static constexpr int kSCols = BLOCK / 16;                          // S / dP column tiles
 };
-static_assert(BwdCfg<64>::kQPerWarp >= 1 && BwdCfg<128>::kQPerWarp >= 1, "dQ tiles per warp");
-static_assert(BwdCfg<64>::kSmem <= 227 * 1024 && BwdCfg<128>::kSmem <= 227 * 1024,
-              "backward SMEM");
+static_assert(BwdCfg<64>::kSmem <= 113 * 1024, "two block-64 backward CTAs per SM");
+static_assert(BwdCfg<128>::kSmem <= 227 * 1024, "backward SMEM");
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
@@ -132,6 +119,53 @@ __device__ __forceinline__ void cp_async_commit() {
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Warp-level tensor-core primitives (the m16n8k16 bf16 mma.sync path, fp32 accumulate).
+// Fragment layout with g = lane / 4, t = lane % 4: an accumulator holds rows g and g + 8,
+// columns 2t and 2t + 1 of a 16 x 8 tile; an A fragment holds rows g, g + 8 and k
+// columns 2t, 2t + 1, 2t + 8, 2t + 9 of a 16 x 16 tile; a B fragment k rows 2t, 2t + 1,
+// 2t + 8, 2t + 9 of column g of a 16 x 8 tile.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p)));
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+      " {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void red_add_v2(float* addr, float x, float y) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(addr), "f"(x), "f"(y) : "memory");
+}
+// ldmatrix row addresses: A (or B stored as [n][k]) from a row-major tile at (r0, c0)
+__device__ __forceinline__ const __nv_bfloat16* frag_a_addr(const __nv_bfloat16* base, int ld,
+                                                            int r0, int c0, uint32_t lane) {
+  return base + (r0 + (int)(lane & 15)) * ld + c0 + (int)(lane >> 4) * 8;
+}
+// two 8-wide n tiles of B stored as [n][k]: rows n0.., k columns k0..k0+15
+__device__ __forceinline__ const __nv_bfloat16* frag_bn_addr(const __nv_bfloat16* base, int ld,
+                                                             int n0, int k0, uint32_t lane) {
+  return base + (n0 + (int)(lane & 7) + (int)(lane >> 4) * 8) * ld + k0 + (int)((lane >> 3) & 1) * 8;
+}
+// two 8-wide n tiles of B stored as [k][n] (transposed load): rows k0.., columns n0..n0+15
+__device__ __forceinline__ const __nv_bfloat16* frag_bk_addr(const __nv_bfloat16* base, int ld,
+                                                             int k0, int n0, uint32_t lane) {
+  return base + (k0 + (int)(lane & 15)) * ld + n0 + (int)(lane >> 4) * 8;
+}
+// A stored transposed as [k][m] (transposed load): rows k0.., columns m0..m0+15
+__device__ __forceinline__ const __nv_bfloat16* frag_at_addr(const __nv_bfloat16* base, int ld,
+                                                             int k0, int m0, uint32_t lane) {
+  return base + (k0 + (int)(lane & 7) + (int)(lane >> 4) * 8) * ld + m0 + (int)((lane >> 3) & 1) * 8;
 }
 
 // rows x 128 bf16 from global (row stride 128) into SMEM with row pitch kLdH, 16 B a time
@@ -165,26 +199,17 @@ __device__ __forceinline__ void prefetch_step(uint8_t* smem, int buf, const BwdA
 }
 
 template <int BLOCK>
-__global__ void __launch_bounds__(BwdCfg<BLOCK>::kThreads, 1) bwd_kv_kernel(const BwdArgs a) {
-  using namespace nvcuda;
+__global__ void __launch_bounds__(BwdCfg<BLOCK>::kThreads) bwd_kv_kernel(const BwdArgs a) {
   using C = BwdCfg<BLOCK>;
-  using FragA = wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::row_major>;
-  using FragAc = wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::col_major>;
-  using FragB = wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::row_major>;
-  using FragBc = wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::col_major>;
-  using FragC = wmma::fragment<wmma::accumulator, 16, 16, 16, float>;
   extern __shared__ __align__(128) uint8_t smem_b[];
-  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(smem_b + C::kOffK);
-  __nv_bfloat16* Vs = reinterpret_cast<__nv_bfloat16*>(smem_b + C::kOffV);
-  float* Sf = reinterpret_cast<float*>(smem_b + C::kOffF);
-  float* dPf = Sf + C::kMq * C::kLdS;
-  float* Of = Sf;  // dQ part / dK / dV staging (after S and dP are consumed)
-  __nv_bfloat16* Pb = reinterpret_cast<__nv_bfloat16*>(smem_b + C::kOffP);
-  __nv_bfloat16* dSb = reinterpret_cast<__nv_bfloat16*>(smem_b + C::kOffDS);
+  const __nv_bfloat16* Ks = reinterpret_cast<const __nv_bfloat16*>(smem_b + C::kOffK);
+  const __nv_bfloat16* Vs = reinterpret_cast<const __nv_bfloat16*>(smem_b + C::kOffV);
+  __nv_bfloat16* dST = reinterpret_cast<__nv_bfloat16*>(smem_b + C::kOffDS);
   uint32_t* steps = reinterpret_cast<uint32_t*>(smem_b + C::kOffList);
   int* n_steps = reinterpret_cast<int*>(smem_b + C::kOffList + (size_t)C::kMaxSteps * 4);
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
+  const int g = (int)(lane >> 2), tq = (int)(lane & 3);
 
   const int kb = blockIdx.x % a.nbk;
   const int bkv = blockIdx.x / a.nbk;  // b * Hkv + hk
@@ -195,17 +220,17 @@ __global__ void __launch_bounds__(BwdCfg<BLOCK>::kThreads, 1) bwd_kv_kernel(cons
     vk = a.vbs[kb];
     vk = vk < 0 ? 0 : (vk > BLOCK ? BLOCK : vk);
   }
-  load_rows<BLOCK>(reinterpret_cast<uint16_t*>(Ks), a.k + krow0 * 128, BLOCK);
-  load_rows<BLOCK>(reinterpret_cast<uint16_t*>(Vs), a.v + krow0 * 128, BLOCK);
+  load_rows<BLOCK>(reinterpret_cast<uint16_t*>(smem_b + C::kOffK), a.k + krow0 * 128, BLOCK);
+  load_rows<BLOCK>(reinterpret_cast<uint16_t*>(smem_b + C::kOffV), a.v + krow0 * 128, BLOCK);
 
-  // this warp's dK and dV tiles: key-row tiles (warp / 8) * kAccPerWarp + i, d column
-  // tile warp % 8
-  FragC dK[C::kAccPerWarp], dV[C::kAccPerWarp];
+  // this warp's 16 keys: rows 16 warp + g and + 8 of the key block
+  const int key0 = 16 * warp + g, key1 = key0 + 8;
+  const bool kv0 = key0 < vk, kv1 = key1 < vk;
+  float dK[16][4], dV[16][4];  // [d tile of 8][fragment]
 #pragma unroll
-  for (int i = 0; i < C::kAccPerWarp; ++i) {
-    wmma::fill_fragment(dK[i], 0.0f);
-    wmma::fill_fragment(dV[i], 0.0f);
-  }
+  for (int i = 0; i < 16; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) dK[i][j] = dV[i][j] = 0.0f;
 
   constexpr int kSub = BLOCK / C::kMq;  // steps per query block
   int scan_h = 0, scan_qb = 0;          // warp 0's position in the (head, query block) scan
@@ -256,113 +281,108 @@ __global__ void __launch_bounds__(BwdCfg<BLOCK>::kThreads, 1) bwd_kv_kernel(cons
           reinterpret_cast<const __nv_bfloat16*>(smem_b + C::kOffDO + buf * C::kQBytes);
       const float* lse_s = reinterpret_cast<const float*>(smem_b + C::kOffRow) + buf * 2 * C::kMq;
       const float* D_s = lse_s + C::kMq;
-      // S = Q K^T and dP = dO V^T: (kMq / 16) x (BLOCK / 16) tiles of each; a warp takes
-      // two column tiles of one row tile of one of them, reusing its A fragment
-      {
-        static_assert(2 * (C::kMq / 16) * C::kSCols == 2 * C::kWarps, "S tiles per warp");
-        const int half = C::kWarps / 2;
-        const bool isdp = warp >= half;
-        const int idx = warp - (isdp ? half : 0);
-        const int tr = idx / (C::kSCols / 2), tc0 = 2 * (idx % (C::kSCols / 2));
-        const __nv_bfloat16* A = isdp ? dOs : Qs;
-        const __nv_bfloat16* Bm = isdp ? Vs : Ks;
-        FragC acc0, acc1;
-        wmma::fill_fragment(acc0, 0.0f);
-        wmma::fill_fragment(acc1, 0.0f);
+      // ---- S^T = K Q^T and dP^T = V dO^T for this warp's 16 keys x kMq queries
+      float sT[4][4], dpT[4][4];
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          FragA fa;
-          FragBc fb0, fb1;  // K^T: column-major views of the row-major K tile
-          wmma::load_matrix_sync(fa, A + tr * 16 * C::kLdH + kk * 16, C::kLdH);
-          wmma::load_matrix_sync(fb0, Bm + tc0 * 16 * C::kLdH + kk * 16, C::kLdH);
-          wmma::load_matrix_sync(fb1, Bm + (tc0 + 1) * 16 * C::kLdH + kk * 16, C::kLdH);
-          wmma::mma_sync(acc0, fa, fb0, acc0);
-          wmma::mma_sync(acc1, fa, fb1, acc1);
-        }
-        float* dst = (isdp ? dPf : Sf) + tr * 16 * C::kLdS + tc0 * 16;
-        wmma::store_matrix_sync(dst, acc0, C::kLdS, wmma::mem_row_major);
-        wmma::store_matrix_sync(dst + 16, acc1, C::kLdS, wmma::mem_row_major);
-      }
-      __syncthreads();
-      // P and dS (dS carries the softmax scale of dq and dk)
-      for (int i = threadIdx.x; i < C::kMq * BLOCK; i += C::kThreads) {
-        const int r = i / BLOCK, j = i - r * BLOCK;
-        const float l2 = lse_s[r];
-        const bool valid = j < vk && l2 > -3.0e38f;  // tail keys; rows with no key
-        const float p = valid ? exp2f(fmaf(Sf[r * C::kLdS + j], a.scale_log2, -l2)) : 0.0f;
-        const float ds = p * (dPf[r * C::kLdS + j] - D_s[r]) * a.scale;
-        Pb[r * C::kLdP + j] = __float2bfloat16_rn(p);
-        dSb[r * C::kLdP + j] = __float2bfloat16_rn(ds);
-      }
-      __syncthreads();
-      // dV += P^T dO and dK += dS^T Q, k over the kMq query rows: this warp's tiles share
-      // one d column tile (so one dO and one Q fragment per k step)
-      {
-        const int tc = warp % 8, tr0 = (warp / 8) * C::kAccPerWarp;
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int kk = 0; kk < C::kMq / 16; ++kk) {
-          FragB fo, fq;
-          wmma::load_matrix_sync(fo, dOs + kk * 16 * C::kLdH + tc * 16, C::kLdH);
-          wmma::load_matrix_sync(fq, Qs + kk * 16 * C::kLdH + tc * 16, C::kLdH);
+        for (int j = 0; j < 4; ++j) sT[i][j] = dpT[i][j] = 0.0f;
 #pragma unroll
-          for (int i = 0; i < C::kAccPerWarp; ++i) {
-            FragAc fp, fds;  // P^T, dS^T: column-major views of row-major P, dS
-            wmma::load_matrix_sync(fp, Pb + kk * 16 * C::kLdP + (tr0 + i) * 16, C::kLdP);
-            wmma::mma_sync(dV[i], fp, fo, dV[i]);
-            wmma::load_matrix_sync(fds, dSb + kk * 16 * C::kLdP + (tr0 + i) * 16, C::kLdP);
-            wmma::mma_sync(dK[i], fds, fq, dK[i]);
-          }
+      for (int kk = 0; kk < 8; ++kk) {  // d in steps of 16
+        uint32_t ak[4], av[4];
+        ldsm_x4(ak, frag_a_addr(Ks, C::kLdH, 16 * warp, 16 * kk, lane));
+        ldsm_x4(av, frag_a_addr(Vs, C::kLdH, 16 * warp, 16 * kk, lane));
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {  // query tiles 2p, 2p + 1
+          uint32_t bq[4], bo[4];
+          ldsm_x4(bq, frag_bn_addr(Qs, C::kLdH, 16 * p, 16 * kk, lane));
+          ldsm_x4(bo, frag_bn_addr(dOs, C::kLdH, 16 * p, 16 * kk, lane));
+          mma16816(sT[2 * p], ak, bq[0], bq[1]);
+          mma16816(sT[2 * p + 1], ak, bq[2], bq[3]);
+          mma16816(dpT[2 * p], av, bo[0], bo[1]);
+          mma16816(dpT[2 * p + 1], av, bo[2], bo[3]);
         }
       }
-      // dQ part = dS K, k over the BLOCK keys (S / dP are dead): this warp's tiles share one
-      // row tile (one dS fragment per k step)
-      {
-        const int base = warp * C::kQPerWarp, tr = base / 8, tc0 = base % 8;
-        FragC acc[C::kQPerWarp];
+      // ---- P^T and dS^T (dS carries the softmax scale of dq and dk), as A fragments
+      uint32_t pA[2][4], dsA[2][4];
 #pragma unroll
-        for (int j = 0; j < C::kQPerWarp; ++j) wmma::fill_fragment(acc[j], 0.0f);
+      for (int nt = 0; nt < 4; ++nt) {
+        float p[4], ds[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int qc = 8 * nt + 2 * tq + (j & 1);
+          const float l2 = lse_s[qc];
+          const bool valid = (j < 2 ? kv0 : kv1) && l2 > -3.0e38f;
+          p[j] = valid ? exp2f(fmaf(sT[nt][j], a.scale_log2, -l2)) : 0.0f;
+          ds[j] = p[j] * (dpT[nt][j] - D_s[qc]) * a.scale;
+        }
+        // accumulator (16 x 8 tile nt) -> half of the A fragment of k step nt / 2
+        pA[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p[0], p[1]);
+        pA[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p[2], p[3]);
+        dsA[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(ds[0], ds[1]);
+        dsA[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+        // dS^T to SMEM for dq: rows key0 / key1, query columns 8 nt + 2 tq, + 1
+        *reinterpret_cast<uint32_t*>(dST + key0 * C::kLdT + 8 * nt + 2 * tq) =
+            dsA[nt >> 1][(nt & 1) * 2 + 0];
+        *reinterpret_cast<uint32_t*>(dST + key1 * C::kLdT + 8 * nt + 2 * tq) =
+            dsA[nt >> 1][(nt & 1) * 2 + 1];
+      }
+      // ---- dV += P^T dO and dK += dS^T Q: k over the kMq queries, n over d
+#pragma unroll
+      for (int j = 0; j < C::kMq / 16; ++j) {
+#pragma unroll
+        for (int dp = 0; dp < 8; ++dp) {  // d tiles 2dp, 2dp + 1
+          uint32_t bo[4], bq[4];
+          ldsm_x4_t(bo, frag_bk_addr(dOs, C::kLdH, 16 * j, 16 * dp, lane));
+          ldsm_x4_t(bq, frag_bk_addr(Qs, C::kLdH, 16 * j, 16 * dp, lane));
+          mma16816(dV[2 * dp], pA[j], bo[0], bo[1]);
+          mma16816(dV[2 * dp + 1], pA[j], bo[2], bo[3]);
+          mma16816(dK[2 * dp], dsA[j], bq[0], bq[1]);
+          mma16816(dK[2 * dp + 1], dsA[j], bq[2], bq[3]);
+        }
+      }
+      __syncthreads();  // dS^T complete
+      // ---- dQ part = dS K: query row tile rt, a range of d tiles, k over the BLOCK keys
+      {
+        constexpr int kRowTiles = C::kMq / 16;                 // 2
+        constexpr int kDTiles = 16 / (C::kWarps / kRowTiles);  // 8 (block 64) or 4 (block 128)
+        const int rt = warp % kRowTiles, d0 = (warp / kRowTiles) * kDTiles;
+        float acc[kDTiles][4];
+#pragma unroll
+        for (int i = 0; i < kDTiles; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
 #pragma unroll
         for (int kk = 0; kk < BLOCK / 16; ++kk) {
-          FragA fa;
-          wmma::load_matrix_sync(fa, dSb + tr * 16 * C::kLdP + kk * 16, C::kLdP);
+          uint32_t ad[4];
+          ldsm_x4_t(ad, frag_at_addr(dST, C::kLdT, 16 * kk, 16 * rt, lane));
 #pragma unroll
-          for (int j = 0; j < C::kQPerWarp; ++j) {
-            FragB fb;
-            wmma::load_matrix_sync(fb, Ks + kk * 16 * C::kLdH + (tc0 + j) * 16, C::kLdH);
-            wmma::mma_sync(acc[j], fa, fb, acc[j]);
+          for (int dp = 0; dp < kDTiles / 2; ++dp) {
+            uint32_t bk[4];
+            ldsm_x4_t(bk, frag_bk_addr(Ks, C::kLdH, 16 * kk, 8 * d0 + 16 * dp, lane));
+            mma16816(acc[2 * dp], ad, bk[0], bk[1]);
+            mma16816(acc[2 * dp + 1], ad, bk[2], bk[3]);
           }
         }
+        float* dst = a.dq_acc + (qrow0 + 16 * rt + g) * 128 + 8 * d0 + 2 * tq;
 #pragma unroll
-        for (int j = 0; j < C::kQPerWarp; ++j)
-          wmma::store_matrix_sync(Of + tr * 16 * C::kLdO + (tc0 + j) * 16, acc[j], C::kLdO,
-                                  wmma::mem_row_major);
+        for (int i = 0; i < kDTiles; ++i) {
+          red_add_v2(dst + 8 * i, acc[i][0], acc[i][1]);
+          red_add_v2(dst + 8 * 128 + 8 * i, acc[i][2], acc[i][3]);
+        }
       }
-      __syncthreads();
-      float* dst = a.dq_acc + qrow0 * 128;
-      for (int i = threadIdx.x; i < C::kMq * 32; i += C::kThreads) {  // 4 floats a time
-        const int r = i >> 5, c4 = (i & 31) * 4;
-        const float4 x = *reinterpret_cast<const float4*>(Of + r * C::kLdO + c4);
-        red_add_v4(dst + r * 128 + c4, x);
-      }
-      __syncthreads();  // Of, P, dS and this step's buffer are free again
+      __syncthreads();  // dS^T and this step's buffer are free again
     }
   }
-  // dK, dV -> bf16, through the fp32 staging area
-  for (int which = 0; which < 2; ++which) {
+  // dK, dV -> bf16: rows key0 / key1, d columns 8 i + 2 tq, + 1
+  uint16_t* dk = a.dk + (krow0 + key0) * 128 + 2 * tq;
+  uint16_t* dv = a.dv + (krow0 + key0) * 128 + 2 * tq;
 #pragma unroll
-    for (int i = 0; i < C::kAccPerWarp; ++i) {
-      const int tr = (warp / 8) * C::kAccPerWarp + i, tc = warp % 8;
-      wmma::store_matrix_sync(Of + tr * 16 * C::kLdO + tc * 16, which ? dV[i] : dK[i], C::kLdO,
-                              wmma::mem_row_major);
-    }
-    __syncthreads();
-    uint16_t* dst = (which ? a.dv : a.dk) + krow0 * 128;
-    for (int i = threadIdx.x; i < BLOCK * 64; i += C::kThreads) {
-      const int r = i >> 6, c2 = (i & 63) * 2;
-      reinterpret_cast<uint32_t*>(dst + r * 128)[c2 >> 1] =
-          pack_bf16x2(Of[r * C::kLdO + c2], Of[r * C::kLdO + c2 + 1]);
-    }
-    __syncthreads();
+  for (int i = 0; i < 16; ++i) {
+    *reinterpret_cast<uint32_t*>(dk + 8 * i) = pack_bf16x2(dK[i][0], dK[i][1]);
+    *reinterpret_cast<uint32_t*>(dk + 8 * 128 + 8 * i) = pack_bf16x2(dK[i][2], dK[i][3]);
+    *reinterpret_cast<uint32_t*>(dv + 8 * i) = pack_bf16x2(dV[i][0], dV[i][1]);
+    *reinterpret_cast<uint32_t*>(dv + 8 * 128 + 8 * i) = pack_bf16x2(dV[i][2], dV[i][3]);
   }
 }
 
