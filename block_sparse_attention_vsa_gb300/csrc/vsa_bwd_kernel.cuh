@@ -54,13 +54,6 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
   if (lane == 0) Dv[r] = acc;
 }
 
-// Four consecutive fp32 atomic adds as one vector reduction (16-byte aligned address).
-__device__ __forceinline__ void red_add_v4(float* addr, float4 x) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(x.x), "f"(x.y),
-               "f"(x.z), "f"(x.w)
-               : "memory");
-}
-
 // fp32 dQ accumulator -> bf16 (round to nearest even), 8 elements per thread.
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ acc,
                                                      long long n8, uint16_t* __restrict__ dq) {
