@@ -441,7 +441,7 @@ def main():
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": TRAFFIC.get(w.name),
                 "peak_source": f"{peak_src} dense bf16 (burst)",
-                "kernel": "bwd_kv_kernel" if bwd else "bsa_fwd_kernel"}
+                "kernel": "bsa_bwd_kernel (whole vsa_bwd call timed)" if bwd else "bsa_fwd_kernel"}
     if bwd:
         roofline["traffic"] = None
 

@@ -355,19 +355,27 @@ BwdLayout bwd_layout(long long B, long long Hq, long long Sq, long long Sk, int 
 }
 
 template <int BLOCK>
-vsa_status launch_bwd(DeviceInfo* dev, const BwdArgs& a, long long n_ctas, cudaStream_t s) {
-  using C = BwdCfg<BLOCK>;
-  auto kern = bwd_kv_kernel<BLOCK>;
+vsa_status launch_bwd(DeviceInfo* dev, const BwdArgs& a, const void* q, const void* k,
+                      const void* v, const void* dout, long long rows_q, long long kv_heads,
+                      long long n_ctas, cudaStream_t s) {
+  auto kern = bwd::bsa_bwd_kernel<BLOCK>;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!dev->bwd_attr_set[BLOCK == 128]) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)C::kSmem) != cudaSuccess)
+                               (int)bwd::kSmemBytes) != cudaSuccess)
         return VSA_ERR_CUDA;
       dev->bwd_attr_set[BLOCK == 128] = true;
     }
   }
-  if (n_ctas > 0) kern<<<(unsigned)n_ctas, C::kThreads, C::kSmem, s>>>(a);
+  if (n_ctas == 0) return VSA_OK;
+  // Q and dO: [rows, 128] with 64-row boxes (a step); K and V: [heads, Sk, 128] with
+  // 128-row boxes clipped at the end of a head (a lone last block-64 key block)
+  CUtensorMap tq, tdo, tk, tv;
+  if (!make_map(&tq, q, rows_q, 64) || !make_map(&tdo, dout, rows_q, 64) ||
+      !make_map_3d(&tk, k, kv_heads, a.Sk) || !make_map_3d(&tv, v, kv_heads, a.Sk))
+    return VSA_ERR_CUDA;
+  kern<<<(unsigned)n_ctas, bwd::kThreads, bwd::kSmemBytes, s>>>(tq, tdo, tk, tv, a);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
@@ -447,11 +455,9 @@ vsa_status vsa_bwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
   if (cudaGetLastError() != cudaSuccess ||
       cudaMemsetAsync(dq_acc, 0, (size_t)rows * 128 * 4, s) != cudaSuccess)
     return VSA_ERR_CUDA;
+  unsigned int* status = status_word();
+  if (status == nullptr) return VSA_ERR_CUDA;
   BwdArgs a{};
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.dout = dout;
   a.lse = lse;
   a.Dv = Dv;
   a.bitmap = bitmap;
@@ -459,6 +465,7 @@ vsa_status vsa_bwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
   a.dq_acc = dq_acc;
   a.dk = dk;
   a.dv = dv;
+  a.status = status;
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.group = Hq / Hkv;
@@ -466,10 +473,12 @@ vsa_status vsa_bwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
   a.Sk = Sk;
   a.nbq = nbq;
   a.nbk = nbk;
+  a.n_tiles = block == 64 ? (nbk + 1) / 2 : nbk;  // key tiles of 128 keys per head
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
-  const long long n_ctas = (long long)B * Hkv * nbk;
-  st = block == 64 ? launch_bwd<64>(dev, a, n_ctas, s) : launch_bwd<128>(dev, a, n_ctas, s);
+  const long long n_ctas = (long long)B * Hkv * a.n_tiles;
+  st = block == 64 ? launch_bwd<64>(dev, a, q, k, v, dout, rows, (long long)B * Hkv, n_ctas, s)
+                   : launch_bwd<128>(dev, a, q, k, v, dout, rows, (long long)B * Hkv, n_ctas, s);
   if (st != VSA_OK) return st;
   if (n_ctas > 0) ++launches;
   const long long n8 = rows * 16;

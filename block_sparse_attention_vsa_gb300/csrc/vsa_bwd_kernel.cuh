@@ -9,27 +9,52 @@
 //   dq_i  = scale sum_j ds_ij k_j,   dk_j = scale sum_i ds_ij q_i,   dv_j = sum_i p_ij dout_i
 // with dk and dv summed over every query head of a key/value group.
 //
-// Structure:
+// Kernels:
 //   bwd_prep_kernel   D_i for every query row (one warp per row).
-//   bwd_kv_kernel     one CTA per (batch, key/value head, key block): K and V of the block
-//                     stay in SMEM; dK and dV accumulate in tensor-core fragments while the
-//                     CTA walks every (query head of the group, query block) that selects
-//                     the key block (a column of the 0/1 block map, compacted into an SMEM
-//                     list), 32 query rows a step, the next step's rows copied in
-//                     asynchronously while the current one computes.  Each warp owns 16
-//                     keys: S^T = K Q^T and dP^T = V dO^T land in its registers, P^T and
-//                     dS^T are formed there and reused as the A operands of dV += P^T dO
-//                     and dK += dS^T Q (dK, dV stay in registers); dS^T goes through SMEM
-//                     for dQ_part = dS K, added to an fp32 dQ accumulator with vector
-//                     reductions (several key blocks feed every query row).
+//   bsa_bwd_kernel    one CTA per (batch, key/value head, key tile of 128 keys): a tile is
+//                     one key block (block 128) or an adjacent pair of key blocks (block
+//                     64: the pair walks the union of the query blocks either selects, and
+//                     keys of a block the query block did not select are masked).  K and V
+//                     of the tile stay in SMEM and dK, dV accumulate in TMEM while the CTA
+//                     walks the (query head of the group, query block) pairs selecting the
+//                     tile -- a column of the 0/1 block map, compacted into an SMEM list --
+//                     64 query rows a step.  Per step, on the 5th-generation tensor cores:
+//                       S^T  = K Q^T      (M = 128 keys, N = 64 queries, K = d) -> TMEM
+//                       dP^T = V dO^T                                           -> TMEM
+//                       P^T, dS^T formed by the gradient warps (one thread per key row)
+//                       and written back over S^T, dP^T as bf16; dS^T also to SMEM
+//                       dV  += P^T dO     (A = P^T from TMEM, B = dO MN-major)
+//                       dK  += dS^T Q     (A = dS^T from TMEM, B = Q MN-major)
+//                       dQ^T = K^T dS^T   (both operands MN-major in SMEM; M = 128 d)
+//                     and the dQ warps add dQ^T (one thread per d column, 64 query rows)
+//                     into an fp32 accumulator with coalesced reductions: several key tiles
+//                     feed every query row.
 //   bwd_dq_kernel     fp32 dQ accumulator -> bf16 dq.
-// The contractions use the warp-level bf16 tensor-core path (mma.sync m16n8k16, fp32
-// accumulation, operands through ldmatrix).
+//
+// bsa_bwd_kernel roles (15 warps):
+//   warps 0-7   gradient warps: warpgroup w handles query columns 32w..32w+31 of a step,
+//               thread = key row (TMEM lane); after the last step they store dV (warps
+//               0-3) and dK (warps 4-7) as bf16.
+//   warps 8-11  dQ warps: thread = d column (TMEM lane of dQ^T).
+//   warp 12     TMA: K, V once; per step Q, dO (64 rows) and lse, D (64 floats) into a
+//               3-stage ring.
+//   warp 13     MMA issuer (one thread); owns the TMEM allocation.
+//   warp 14     list: compacts the block-map column into the step list (in chunks).
+// TMEM (512 columns): S^T 0-63 (P^T bf16 over 0-15 and 32-47), dP^T 64-127 (dS^T over
+// 64-79 and 96-111), dQ^T double buffer 128-255, dV 256-383, dK 384-511.
+// MMA issue order per step t: dV_t, S_{t+1}, dK_t, dQ_t, dP_{t+1}.  tcgen05 MMAs of one
+// thread execute in issue order, so S_{t+1} may overwrite the P^T that dV_t reads and
+// dP_{t+1} the dS^T that dK_t reads; the commit behind S_{t+1} (dP_{t+1}) tells the
+// gradient warps both that S^T (dP^T) is ready and that its previous readers are done.
+// Every mbarrier wait is bounded; a wait that runs out records a code in the device
+// status word, raises the CTA's abort flag and every role returns.
 #pragma once
 
-#include <cuda_bf16.h>
+#include <cuda.h>
 
 #include <cstdint>
+
+#include "sm103_ptx.cuh"
 
 namespace vsa {
 
@@ -70,313 +95,494 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ a
 }
 
 struct BwdArgs {
-  const uint16_t *q, *k, *v, *dout;
   const float* lse;         // [B*Hq*Sq], base 2, from the forward
   const float* Dv;          // [B*Hq*Sq]
   const int8_t* bitmap;     // [B*Hq*nbq, nbk] 0/1 block map
   const int32_t* vbs;       // [nbk] or null
   float* dq_acc;            // [B*Hq*Sq, 128] fp32, zeroed
   uint16_t *dk, *dv;        // [B*Hkv*Sk, 128] bf16
+  unsigned int* status;     // device status word
   int Hq, Hkv, group, Sq, Sk, nbq, nbk;
+  int n_tiles;              // key tiles (of 128 keys) per key/value head
   float scale, scale_log2;
 };
 
-template <int BLOCK>
-struct BwdCfg {
-  static constexpr int kWarps = BLOCK / 16;          // one warp per 16 keys: 4 or 8
-  static constexpr int kThreads = kWarps * 32;
-  static constexpr int kMq = 32;                     // query rows per step
-  static constexpr int kLdH = 128 + 8;               // bf16 row pitch of K, V, Q, dO tiles
-  static constexpr int kLdT = kMq + 8;               // bf16 row pitch of the dS^T tile
-  static constexpr int kMaxSteps = 2048;             // (query head, query block) list chunk
-  static constexpr size_t kQBytes = (size_t)kMq * kLdH * 2;
-  static constexpr size_t kOffK = 0;
-  static constexpr size_t kOffV = kOffK + (size_t)BLOCK * kLdH * 2;
-  static constexpr size_t kOffQ = kOffV + (size_t)BLOCK * kLdH * 2;   // Q[2]
-  static constexpr size_t kOffDO = kOffQ + 2 * kQBytes;                // dO[2]
-  static constexpr size_t kOffDS = kOffDO + 2 * kQBytes;               // dS^T [BLOCK][kLdT]
-  static constexpr size_t kOffRow = kOffDS + (size_t)BLOCK * kLdT * 2; // [2] x (lse, D)[kMq]
-  static constexpr size_t kOffList = kOffRow + 2 * 2 * kMq * 4;
-  static constexpr size_t kSmem = kOffList + (size_t)kMaxSteps * 4 + 16;
+namespace bwd {
+
+constexpr int kThreads = 480;
+constexpr int kStages = 3;
+constexpr int kMaxEntries = 2048;  // (query head, query block) list chunk
+constexpr int kDqWarp0 = 8, kTmaWarp = 12, kMmaWarp = 13, kListWarp = 14;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per wait
+constexpr unsigned kErrTimeout = 0x100u;           // | code of the wait that gave up
+
+// shared-memory map (bytes from a 1024-aligned base); every operand tile is stored as
+// 64-column (128-byte) halves with the 128-byte swizzle, as TMA writes them
+constexpr uint32_t kKVTile = 128 * 128 * 2;  // K or V: [2 d-halves][128 keys][64]
+constexpr uint32_t kQTile = 64 * 128 * 2;    // Q or dO of a step: [2 d-halves][64 rows][64]
+constexpr uint32_t kOffK = 0;
+constexpr uint32_t kOffV = kKVTile;
+constexpr uint32_t kOffQ = 2 * kKVTile;                  // [kStages]
+constexpr uint32_t kOffDO = kOffQ + kStages * kQTile;    // [kStages]
+constexpr uint32_t kOffDS = kOffDO + kStages * kQTile;   // dS^T [128 keys][64 queries] bf16
+constexpr uint32_t kOffRow = kOffDS + 128 * 64 * 2;      // [kStages] lse[64], D[64]
+constexpr uint32_t kOffList = kOffRow + kStages * 512;
+constexpr uint32_t kOffCtl = kOffList + kMaxEntries * 4;
+constexpr uint32_t kSmemBytes = kOffCtl + 1024 + 1024;  // + alignment slack
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kColDV = 256, kColDK = 384;
+
+struct Ctl {
+  uint64_t kv_full;
+  uint64_t ld_full[kStages], ld_empty[kStages];
+  uint64_t s_full, dp_full;  // S^T (dP^T) of the step is in TMEM; its previous readers are done
+  uint64_t p_full, ds_full;  // the 8 gradient warps wrote P^T (dS^T)
+  uint64_t dq_full[2], dq_empty[2];
+  uint64_t acc_full, drain;
+  int n_entries, go;
+  uint32_t tmem_base;
+  int abort_flag;
 };
-static_assert(BwdCfg<64>::kSmem <= 113 * 1024, "two block-64 backward CTAs per SM");
-static_assert(BwdCfg<128>::kSmem <= 227 * 1024, "backward SMEM");
+static_assert(sizeof(Ctl) <= 1024, "control block too large");
+static_assert(kOffDS % 1024 == 0 && kOffQ % 1024 == 0 && kOffDO % 1024 == 0, "swizzle atoms");
+static_assert(kSmemBytes <= 227 * 1024, "backward SMEM");
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Warp-level tensor-core primitives (the m16n8k16 bf16 mma.sync path, fp32 accumulate).
-// Fragment layout with g = lane / 4, t = lane % 4: an accumulator holds rows g and g + 8,
-// columns 2t and 2t + 1 of a 16 x 8 tile; an A fragment holds rows g, g + 8 and k
-// columns 2t, 2t + 1, 2t + 8, 2t + 9 of a 16 x 16 tile; a B fragment k rows 2t, 2t + 1,
-// 2t + 8, 2t + 9 of column g of a 16 x 8 tile.
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_addr(p)));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_addr(p)));
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
-      " {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void red_add_v2(float* addr, float x, float y) {
-  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(addr), "f"(x), "f"(y) : "memory");
-}
-// ldmatrix row addresses: A (or B stored as [n][k]) from a row-major tile at (r0, c0)
-__device__ __forceinline__ const __nv_bfloat16* frag_a_addr(const __nv_bfloat16* base, int ld,
-                                                            int r0, int c0, uint32_t lane) {
-  return base + (r0 + (int)(lane & 15)) * ld + c0 + (int)(lane >> 4) * 8;
-}
-// two 8-wide n tiles of B stored as [n][k]: rows n0.., k columns k0..k0+15
-__device__ __forceinline__ const __nv_bfloat16* frag_bn_addr(const __nv_bfloat16* base, int ld,
-                                                             int n0, int k0, uint32_t lane) {
-  return base + (n0 + (int)(lane & 7) + (int)(lane >> 4) * 8) * ld + k0 + (int)((lane >> 3) & 1) * 8;
-}
-// two 8-wide n tiles of B stored as [k][n] (transposed load): rows k0.., columns n0..n0+15
-__device__ __forceinline__ const __nv_bfloat16* frag_bk_addr(const __nv_bfloat16* base, int ld,
-                                                             int k0, int n0, uint32_t lane) {
-  return base + (k0 + (int)(lane & 15)) * ld + n0 + (int)(lane >> 4) * 8;
-}
-// A stored transposed as [k][m] (transposed load): rows k0.., columns m0..m0+15
-__device__ __forceinline__ const __nv_bfloat16* frag_at_addr(const __nv_bfloat16* base, int ld,
-                                                             int k0, int m0, uint32_t lane) {
-  return base + (k0 + (int)(lane & 7) + (int)(lane >> 4) * 8) * ld + m0 + (int)((lane >> 3) & 1) * 8;
-}
-
-// rows x 128 bf16 from global (row stride 128) into SMEM with row pitch kLdH, 16 B a time
-template <int BLOCK>
-__device__ __forceinline__ void load_rows(uint16_t* dst, const uint16_t* src, int rows) {
-  using C = BwdCfg<BLOCK>;
-  for (int i = threadIdx.x; i < rows * 16; i += C::kThreads) {
-    const int r = i >> 4, c = i & 15;
-    reinterpret_cast<uint4*>(dst + r * C::kLdH)[c] = reinterpret_cast<const uint4*>(src + r * 128)[c];
-  }
-}
-
-// Asynchronous copy of one step's inputs: kMq rows of Q and dO, their lse and D.
-template <int BLOCK>
-__device__ __forceinline__ void prefetch_step(uint8_t* smem, int buf, const BwdArgs& a,
-                                              long long qrow0) {
-  using C = BwdCfg<BLOCK>;
-  uint8_t* qd = smem + C::kOffQ + buf * C::kQBytes;
-  uint8_t* od = smem + C::kOffDO + buf * C::kQBytes;
-  for (int i = threadIdx.x; i < C::kMq * 16; i += C::kThreads) {
-    const int r = i >> 4, c = i & 15;
-    cp_async16(qd + (r * C::kLdH + c * 8) * 2, a.q + (qrow0 + r) * 128 + c * 8);
-    cp_async16(od + (r * C::kLdH + c * 8) * 2, a.dout + (qrow0 + r) * 128 + c * 8);
-  }
-  float* row = reinterpret_cast<float*>(smem + C::kOffRow) + buf * 2 * C::kMq;
-  for (int i = threadIdx.x; i < C::kMq / 4; i += C::kThreads) {
-    cp_async16(row + 4 * i, a.lse + qrow0 + 4 * i);
-    cp_async16(row + C::kMq + 4 * i, a.Dv + qrow0 + 4 * i);
-  }
-  cp_async_commit();
-}
-
-template <int BLOCK>
-__global__ void __launch_bounds__(BwdCfg<BLOCK>::kThreads) bwd_kv_kernel(const BwdArgs a) {
-  using C = BwdCfg<BLOCK>;
-  extern __shared__ __align__(128) uint8_t smem_b[];
-  const __nv_bfloat16* Ks = reinterpret_cast<const __nv_bfloat16*>(smem_b + C::kOffK);
-  const __nv_bfloat16* Vs = reinterpret_cast<const __nv_bfloat16*>(smem_b + C::kOffV);
-  __nv_bfloat16* dST = reinterpret_cast<__nv_bfloat16*>(smem_b + C::kOffDS);
-  uint32_t* steps = reinterpret_cast<uint32_t*>(smem_b + C::kOffList);
-  int* n_steps = reinterpret_cast<int*>(smem_b + C::kOffList + (size_t)C::kMaxSteps * 4);
-  const int warp = threadIdx.x >> 5;
-  const uint32_t lane = threadIdx.x & 31;
-  const int g = (int)(lane >> 2), tq = (int)(lane & 3);
-
-  const int kb = blockIdx.x % a.nbk;
-  const int bkv = blockIdx.x / a.nbk;  // b * Hkv + hk
-  const int b = bkv / a.Hkv, hk = bkv - b * a.Hkv;
-  const long long krow0 = (long long)bkv * a.Sk + (long long)kb * BLOCK;
-  int vk = BLOCK;
-  if (a.vbs != nullptr) {
-    vk = a.vbs[kb];
-    vk = vk < 0 ? 0 : (vk > BLOCK ? BLOCK : vk);
-  }
-  load_rows<BLOCK>(reinterpret_cast<uint16_t*>(smem_b + C::kOffK), a.k + krow0 * 128, BLOCK);
-  load_rows<BLOCK>(reinterpret_cast<uint16_t*>(smem_b + C::kOffV), a.v + krow0 * 128, BLOCK);
-
-  // this warp's 16 keys: rows 16 warp + g and + 8 of the key block
-  const int key0 = 16 * warp + g, key1 = key0 + 8;
-  const bool kv0 = key0 < vk, kv1 = key1 < vk;
-  float dK[16][4], dV[16][4];  // [d tile of 8][fragment]
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) dK[i][j] = dV[i][j] = 0.0f;
-
-  constexpr int kSub = BLOCK / C::kMq;  // steps per query block
-  int scan_h = 0, scan_qb = 0;          // warp 0's position in the (head, query block) scan
+// Bounded wait on an mbarrier phase (as in the forward): gives up after kWaitLimitNs,
+// recording `code` in the status word and raising the abort flag, or as soon as another
+// role has raised the flag -- unless `drain`, for copies / MMAs still in flight.
+__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, Ctl* ctl, unsigned* status,
+                                     unsigned code, bool drain = false) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
   while (true) {
-    // ---- the next chunk of (query head, query block) pairs selecting this key block:
-    // a column of the block map, compacted in order by warp 0
-    __syncthreads();  // the previous chunk is done with the list
-    if (warp == 0) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (!drain && *reinterpret_cast<volatile int*>(&ctl->abort_flag)) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
+      atomicCAS(status, 0u, kErrTimeout | code);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void red_add_f32(float* addr, float x) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(x) : "memory");
+}
+
+// list entry: bits 0-15 query block, bits 16-17 which key block(s) of the tile it
+// selects, bits 20-31 query head within the group.  First query row of step `sub`.
+__device__ __forceinline__ long long entry_row0(uint32_t e, int sub, const BwdArgs& a, int b,
+                                                int hk, int block) {
+  const long long bh = (long long)b * a.Hq + hk * a.group + (int)(e >> 20);
+  return bh * a.Sq + (long long)(e & 0xFFFFu) * block + sub * 64;
+}
+
+template <int BLOCK>
+__global__ void __launch_bounds__(kThreads, 1)
+    bsa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
+                   const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                   const BwdArgs a) {
+  constexpr int kSubQ = BLOCK / 64;  // steps per list entry
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + kOffCtl);
+  uint32_t* list = reinterpret_cast<uint32_t*>(smem + kOffList);
+  const int warp = (int)(threadIdx.x >> 5);
+  const uint32_t lane = threadIdx.x & 31;
+
+  const int tile = (int)(blockIdx.x % (unsigned)a.n_tiles);
+  const int bkv = (int)(blockIdx.x / (unsigned)a.n_tiles);  // b * Hkv + hk
+  const int b = bkv / a.Hkv, hk = bkv - b * a.Hkv;
+  // valid keys of the tile's key block(s): vk[i] for key rows 64 i .. (block 64)
+  int vk[2] = {0, 0};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int kb = BLOCK == 64 ? 2 * tile + i : tile;
+    if ((BLOCK == 64 || i == 0) && kb < a.nbk) {
+      const int v = a.vbs != nullptr ? a.vbs[kb] : BLOCK;
+      vk[i] = v < 0 ? 0 : (v > BLOCK ? BLOCK : v);
+    }
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl->kv_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctl->ld_full[s], 1);
+      mbar_init(&ctl->ld_empty[s], 1);
+    }
+    mbar_init(&ctl->s_full, 1);
+    mbar_init(&ctl->dp_full, 1);
+    mbar_init(&ctl->p_full, 8);
+    mbar_init(&ctl->ds_full, 8);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->dq_full[i], 1);
+      mbar_init(&ctl->dq_empty[i], 4);
+    }
+    mbar_init(&ctl->acc_full, 1);
+    mbar_init(&ctl->drain, 1);
+    ctl->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tdo);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&ctl->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;  // the warp's TMEM lanes
+
+  uint32_t g = 0;               // steps so far (every role counts alike)
+  int scan_h = 0, scan_qb = 0;  // list warp: position in the (head, query block) scan
+  bool kv_issued = false;       // TMA warp
+  uint32_t fills[kStages] = {0, 0, 0};
+  bool ok = true;               // this role has not given up
+  while (true) {
+    __syncthreads();  // every role is done with the previous chunk's list
+    if (warp == kListWarp) {
+      // the column of the block map: (query head h of the group, query block qb) pairs
+      // that select the tile's key block(s), ascending, 128 query blocks per round trip
       int cnt = 0;
-      while (scan_h < a.group && cnt + 32 <= C::kMaxSteps) {
+      while (scan_h < a.group && cnt + 128 <= kMaxEntries) {
         const long long bh = (long long)b * a.Hq + hk * a.group + scan_h;
-        const int qb = scan_qb + (int)lane;
-        const bool sel = qb < a.nbq && a.bitmap[(bh * a.nbq + qb) * (long long)a.nbk + kb] != 0;
-        const uint32_t ballot = __ballot_sync(0xffffffffu, sel);
-        if (sel) steps[cnt + __popc(ballot & ((1u << lane) - 1u))] = ((uint32_t)scan_h << 20) | qb;
-        cnt += __popc(ballot);
-        scan_qb += 32;
+        uint32_t sel[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int qb = scan_qb + 32 * u + (int)lane;
+          sel[u] = 0;
+          if (qb < a.nbq) {
+            const int8_t* row = a.bitmap + (bh * a.nbq + qb) * (long long)a.nbk;
+            if (BLOCK == 128) {
+              sel[u] = row[tile] != 0 ? 1u : 0u;
+            } else {
+              sel[u] = row[2 * tile] != 0 ? 1u : 0u;
+              if (2 * tile + 1 < a.nbk && row[2 * tile + 1] != 0) sel[u] |= 2u;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t ballot = __ballot_sync(0xffffffffu, sel[u] != 0);
+          if (sel[u])
+            list[cnt + __popc(ballot & ((1u << lane) - 1u))] =
+                ((uint32_t)scan_h << 20) | (sel[u] << 16) | (uint32_t)(scan_qb + 32 * u + lane);
+          cnt += __popc(ballot);
+        }
+        scan_qb += 128;
         if (scan_qb >= a.nbq) {
           scan_qb = 0;
           ++scan_h;
         }
       }
-      if (lane == 0) *n_steps = cnt;
+      if (lane == 0) {
+        ctl->n_entries = cnt;
+        ctl->go = (cnt > 0 && *reinterpret_cast<volatile int*>(&ctl->abort_flag) == 0) ? 1 : 0;
+      }
     }
     __syncthreads();
-    const int n = *n_steps;
-    if (n == 0) break;
-    const int total = n * kSub;
-    auto step_row = [&](int s) -> long long {
-      const uint32_t e = steps[s / kSub];
-      const long long bh = (long long)b * a.Hq + hk * a.group + (int)(e >> 20);
-      return bh * a.Sq + (long long)(e & 0xFFFFFu) * BLOCK + (s % kSub) * C::kMq;
-    };
-    prefetch_step<BLOCK>(smem_b, 0, a, step_row(0));
-    for (int s = 0; s < total; ++s) {
-      const int buf = s & 1;
-      const long long qrow0 = step_row(s);
-      if (s + 1 < total) {
-        prefetch_step<BLOCK>(smem_b, buf ^ 1, a, step_row(s + 1));
-        cp_async_wait<1>();
-      } else {
-        cp_async_wait<0>();
-      }
-      __syncthreads();  // this step's inputs have landed for every thread
-      const __nv_bfloat16* Qs =
-          reinterpret_cast<const __nv_bfloat16*>(smem_b + C::kOffQ + buf * C::kQBytes);
-      const __nv_bfloat16* dOs =
-          reinterpret_cast<const __nv_bfloat16*>(smem_b + C::kOffDO + buf * C::kQBytes);
-      const float* lse_s = reinterpret_cast<const float*>(smem_b + C::kOffRow) + buf * 2 * C::kMq;
-      const float* D_s = lse_s + C::kMq;
-      // ---- S^T = K Q^T and dP^T = V dO^T for this warp's 16 keys x kMq queries
-      float sT[4][4], dpT[4][4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) sT[i][j] = dpT[i][j] = 0.0f;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {  // d in steps of 16
-        uint32_t ak[4], av[4];
-        ldsm_x4(ak, frag_a_addr(Ks, C::kLdH, 16 * warp, 16 * kk, lane));
-        ldsm_x4(av, frag_a_addr(Vs, C::kLdH, 16 * warp, 16 * kk, lane));
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {  // query tiles 2p, 2p + 1
-          uint32_t bq[4], bo[4];
-          ldsm_x4(bq, frag_bn_addr(Qs, C::kLdH, 16 * p, 16 * kk, lane));
-          ldsm_x4(bo, frag_bn_addr(dOs, C::kLdH, 16 * p, 16 * kk, lane));
-          mma16816(sT[2 * p], ak, bq[0], bq[1]);
-          mma16816(sT[2 * p + 1], ak, bq[2], bq[3]);
-          mma16816(dpT[2 * p], av, bo[0], bo[1]);
-          mma16816(dpT[2 * p + 1], av, bo[2], bo[3]);
+    if (!ctl->go) break;
+    const int n_steps = ctl->n_entries * kSubQ;
+    const uint32_t g0 = g;
+    g += (uint32_t)n_steps;
+    if (!ok) continue;
+
+    if (warp == kTmaWarp) {
+      // ---------------------------------------------------------------- copies
+      if (lane == 0) {
+        if (!kv_issued) {
+          const uint64_t pol = policy_evict_first();
+          mbar_arrive_expect_tx(&ctl->kv_full, 2 * kKVTile);
+          tma_load_3d_hint(smem + kOffK, &tk, &ctl->kv_full, 0, 128 * tile, bkv, pol);
+          tma_load_3d_hint(smem + kOffK + kKVTile / 2, &tk, &ctl->kv_full, 64, 128 * tile, bkv,
+                           pol);
+          tma_load_3d_hint(smem + kOffV, &tv, &ctl->kv_full, 0, 128 * tile, bkv, pol);
+          tma_load_3d_hint(smem + kOffV + kKVTile / 2, &tv, &ctl->kv_full, 64, 128 * tile, bkv,
+                           pol);
+          kv_issued = true;
+        }
+        for (int i = 0; i < n_steps; ++i) {
+          const uint32_t gg = g0 + i, st = gg % kStages;
+          if (gg >= (uint32_t)kStages &&
+              !wait(&ctl->ld_empty[st], ((gg / kStages) + 1) & 1, ctl, a.status, 0x41)) {
+            ok = false;
+            break;
+          }
+          const long long row0 = entry_row0(list[i / kSubQ], i % kSubQ, a, b, hk, BLOCK);
+          uint8_t* qs = smem + kOffQ + st * kQTile;
+          uint8_t* os = smem + kOffDO + st * kQTile;
+          float* rs = reinterpret_cast<float*>(smem + kOffRow + st * 512);
+          mbar_arrive_expect_tx(&ctl->ld_full[st], 2 * kQTile + 512);
+          tma_load_2d(qs, &tq, &ctl->ld_full[st], 0, (int)row0);
+          tma_load_2d(qs + kQTile / 2, &tq, &ctl->ld_full[st], 64, (int)row0);
+          tma_load_2d(os, &tdo, &ctl->ld_full[st], 0, (int)row0);
+          tma_load_2d(os + kQTile / 2, &tdo, &ctl->ld_full[st], 64, (int)row0);
+          bulk_load(rs, a.lse + row0, 256, &ctl->ld_full[st]);
+          bulk_load(rs + 64, a.Dv + row0, 256, &ctl->ld_full[st]);
+          ++fills[st];
         }
       }
-      // ---- P^T and dS^T (dS carries the softmax scale of dq and dk), as A fragments
-      uint32_t pA[2][4], dsA[2][4];
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    } else if (warp == kMmaWarp) {
+      // ---------------------------------------------------------------- MMA issue
+      if (lane == 0) {
+        constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);
+        constexpr uint32_t kIdescG = idesc_bf16_f32(128, 128, false, true);
+        constexpr uint32_t kIdescQ = idesc_bf16_f32(128, 64, true, true);
+        const uint64_t k_kmaj = smem_desc_sw128(smem_addr(smem + kOffK), 16, 1024);
+        const uint64_t v_kmaj = smem_desc_sw128(smem_addr(smem + kOffV), 16, 1024);
+        const uint64_t k_mn = smem_desc_sw128(smem_addr(smem + kOffK), kKVTile / 2, 1024);
+        const uint64_t ds_mn = smem_desc_sw128(smem_addr(smem + kOffDS), 8192, 1024);
+        if (g0 == 0 && !wait(&ctl->kv_full, 0, ctl, a.status, 0x42)) ok = false;
+        // S^T (dP^T) of step gg: A = K (V) K-major, B = Q (dO) K-major, K = d in 8 steps
+        auto issue_sd = [&](uint32_t gg, bool dp) {
+          const uint32_t st = gg % kStages;
+          const uint64_t ad = dp ? v_kmaj : k_kmaj;
+          const uint64_t bd =
+              smem_desc_sw128(smem_addr(smem + (dp ? kOffDO : kOffQ) + st * kQTile), 16, 1024);
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        float p[4], ds[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int qc = 8 * nt + 2 * tq + (j & 1);
-          const float l2 = lse_s[qc];
-          const bool valid = (j < 2 ? kv0 : kv1) && l2 > -3.0e38f;
-          p[j] = valid ? exp2f(fmaf(sT[nt][j], a.scale_log2, -l2)) : 0.0f;
-          ds[j] = p[j] * (dpT[nt][j] - D_s[qc]) * a.scale;
-        }
-        // accumulator (16 x 8 tile nt) -> half of the A fragment of k step nt / 2
-        pA[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p[0], p[1]);
-        pA[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p[2], p[3]);
-        dsA[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(ds[0], ds[1]);
-        dsA[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(ds[2], ds[3]);
-        // dS^T to SMEM for dq: rows key0 / key1, query columns 8 nt + 2 tq, + 1
-        *reinterpret_cast<uint32_t*>(dST + key0 * C::kLdT + 8 * nt + 2 * tq) =
-            dsA[nt >> 1][(nt & 1) * 2 + 0];
-        *reinterpret_cast<uint32_t*>(dST + key1 * C::kLdT + 8 * nt + 2 * tq) =
-            dsA[nt >> 1][(nt & 1) * 2 + 1];
-      }
-      // ---- dV += P^T dO and dK += dS^T Q: k over the kMq queries, n over d
-#pragma unroll
-      for (int j = 0; j < C::kMq / 16; ++j) {
-#pragma unroll
-        for (int dp = 0; dp < 8; ++dp) {  // d tiles 2dp, 2dp + 1
-          uint32_t bo[4], bq[4];
-          ldsm_x4_t(bo, frag_bk_addr(dOs, C::kLdH, 16 * j, 16 * dp, lane));
-          ldsm_x4_t(bq, frag_bk_addr(Qs, C::kLdH, 16 * j, 16 * dp, lane));
-          mma16816(dV[2 * dp], pA[j], bo[0], bo[1]);
-          mma16816(dV[2 * dp + 1], pA[j], bo[2], bo[3]);
-          mma16816(dK[2 * dp], dsA[j], bq[0], bq[1]);
-          mma16816(dK[2 * dp + 1], dsA[j], bq[2], bq[3]);
-        }
-      }
-      __syncthreads();  // dS^T complete
-      // ---- dQ part = dS K: query row tile rt, a range of d tiles, k over the BLOCK keys
-      {
-        constexpr int kRowTiles = C::kMq / 16;                 // 2
-        constexpr int kDTiles = 16 / (C::kWarps / kRowTiles);  // 8 (block 64) or 4 (block 128)
-        const int rt = warp % kRowTiles, d0 = (warp / kRowTiles) * kDTiles;
-        float acc[kDTiles][4];
-#pragma unroll
-        for (int i = 0; i < kDTiles; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
-#pragma unroll
-        for (int kk = 0; kk < BLOCK / 16; ++kk) {
-          uint32_t ad[4];
-          ldsm_x4_t(ad, frag_at_addr(dST, C::kLdT, 16 * kk, 16 * rt, lane));
-#pragma unroll
-          for (int dp = 0; dp < kDTiles / 2; ++dp) {
-            uint32_t bk[4];
-            ldsm_x4_t(bk, frag_bk_addr(Ks, C::kLdH, 16 * kk, 8 * d0 + 16 * dp, lane));
-            mma16816(acc[2 * dp], ad, bk[0], bk[1]);
-            mma16816(acc[2 * dp + 1], ad, bk[2], bk[3]);
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t oa = ((k >> 2) * (kKVTile / 2) + (k & 3) * 32) >> 4;
+            const uint64_t ob = ((k >> 2) * (kQTile / 2) + (k & 3) * 32) >> 4;
+            mma_ss(tmem + (dp ? kColDP : kColS), ad + oa, bd + ob, kIdescS, k > 0 ? 1u : 0u);
+          }
+        };
+        if (ok) {
+          if (!wait(&ctl->ld_full[g0 % kStages], (g0 / kStages) & 1, ctl, a.status, 0x43)) {
+            ok = false;
+          } else {
+            tc_fence_after();
+            issue_sd(g0, false);
+            mma_commit(&ctl->s_full);
+            issue_sd(g0, true);
+            mma_commit(&ctl->dp_full);
           }
         }
-        float* dst = a.dq_acc + (qrow0 + 16 * rt + g) * 128 + 8 * d0 + 2 * tq;
+        for (int i = 0; i < n_steps && ok; ++i) {
+          const uint32_t gg = g0 + i, st = gg % kStages;
+          // dV += P^T dO: A = P^T (TMEM, 64 query columns as 32 packed), B = dO MN-major
+          if (!wait(&ctl->p_full, gg & 1, ctl, a.status, 0x44)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t do_mn =
+              smem_desc_sw128(smem_addr(smem + kOffDO + st * kQTile), kQTile / 2, 1024);
 #pragma unroll
-        for (int i = 0; i < kDTiles; ++i) {
-          red_add_v2(dst + 8 * i, acc[i][0], acc[i][1]);
-          red_add_v2(dst + 8 * 128 + 8 * i, acc[i][2], acc[i][3]);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + kColDV, tmem + kColS + 32 * (kk >> 1) + 8 * (kk & 1),
+                   do_mn + ((kk * 2048) >> 4), kIdescG, (gg > 0 || kk > 0) ? 1u : 0u);
+          if (i + 1 < n_steps) {  // S^T of the next step
+            const uint32_t gn = gg + 1;
+            if (!wait(&ctl->ld_full[gn % kStages], (gn / kStages) & 1, ctl, a.status, 0x45)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_sd(gn, false);
+            mma_commit(&ctl->s_full);
+          }
+          // dK += dS^T Q
+          if (!wait(&ctl->ds_full, gg & 1, ctl, a.status, 0x46)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t q_mn =
+              smem_desc_sw128(smem_addr(smem + kOffQ + st * kQTile), kQTile / 2, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + kColDK, tmem + kColDP + 32 * (kk >> 1) + 8 * (kk & 1),
+                   q_mn + ((kk * 2048) >> 4), kIdescG, (gg > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&ctl->ld_empty[st]);  // Q, dO, lse, D of the stage consumed
+          // dQ^T = K^T dS^T into dQ buffer gg & 1, K = keys in 8 steps
+          const uint32_t db = gg & 1;
+          if (gg >= 2 && !wait(&ctl->dq_empty[db], ((gg >> 1) + 1) & 1, ctl, a.status, 0x47)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ss(tmem + kColDQ + 64 * db, k_mn + ((k * 2048) >> 4), ds_mn + ((k * 2048) >> 4),
+                   kIdescQ, k > 0 ? 1u : 0u);
+          mma_commit(&ctl->dq_full[db]);
+          if (i + 1 < n_steps) {  // dP^T of the next step (its copies have landed)
+            issue_sd(gg + 1, true);
+            mma_commit(&ctl->dp_full);
+          }
         }
       }
-      __syncthreads();  // dS^T and this step's buffer are free again
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    } else if (warp < 8) {
+      // ---------------------------------------------------------------- P^T and dS^T
+      const int wg = warp >> 2;
+      const int r = (warp & 3) * 32 + (int)lane;  // key row of the tile
+      const int kbi = BLOCK == 64 ? (r >> 6) : 0;
+      const bool key_ok = (r & (BLOCK - 1)) < vk[kbi];
+      uint8_t* ds_row = smem + kOffDS + (r >> 3) * 1024 + (r & 7) * 128;
+      for (int i = 0; i < n_steps; ++i) {
+        const uint32_t gg = g0 + i, st = gg % kStages;
+        const uint32_t e = list[i / kSubQ];
+        const bool valid = key_ok && ((e >> (16 + kbi)) & 1u);
+        const float* lse_s = reinterpret_cast<const float*>(smem + kOffRow + st * 512) + 32 * wg;
+        const float* D_s = lse_s + 64;
+        // lse and D of the step have landed (the stage is not refilled before dK of this
+        // step, which waits for this warp), and S^T is in TMEM
+        if (!wait(&ctl->ld_full[st], (gg / kStages) & 1, ctl, a.status, 0x48) ||
+            !wait(&ctl->s_full, gg & 1, ctl, a.status, 0x49)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + kColS + 32 * wg, sr);
+        tmem_wait_ld();
+        float p[32];
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 l4 = reinterpret_cast<const float4*>(lse_s)[c4];
+          const float l[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = 4 * c4 + j;
+            p[c] = (valid && l[j] > -3.0e38f)
+                       ? fast_exp2(fmaf(__uint_as_float(sr[c]), a.scale_log2, -l[j]))
+                       : 0.0f;
+          }
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
+        tmem_st_32x32b_x16(tmem + lane_base + kColS + 32 * wg, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->p_full);
+        if (!wait(&ctl->dp_full, gg & 1, ctl, a.status, 0x4a)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_ld_32x32b_x32(tmem + lane_base + kColDP + 32 * wg, sr);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 d4 = reinterpret_cast<const float4*>(D_s)[c4];
+          const float d[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = 4 * c4 + j;
+            p[c] = p[c] * (__uint_as_float(sr[c]) - d[j]) * a.scale;  // dS, scaled
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
+        tmem_st_32x32b_x16(tmem + lane_base + kColDP + 32 * wg, pk);
+        // dS^T row r, query columns 32 wg .. 32 wg + 31: 16-byte chunks 4 wg .. 4 wg + 3
+        // of the 128-byte row, placed by the 128-byte swizzle (chunk ^ row % 8)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int phys = (4 * wg + c) ^ (r & 7);
+          *reinterpret_cast<uint4*>(ds_row + phys * 16) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->ds_full);
+      }
+    } else if (warp >= kDqWarp0 && warp < kDqWarp0 + 4) {
+      // ---------------------------------------------------------------- dQ reductions
+      const int d = (warp & 3) * 32 + (int)lane;  // d column (TMEM lane of dQ^T)
+      for (int i = 0; i < n_steps; ++i) {
+        const uint32_t gg = g0 + i, db = gg & 1;
+        const long long row0 = entry_row0(list[i / kSubQ], i % kSubQ, a, b, hk, BLOCK);
+        if (!wait(&ctl->dq_full[db], (gg >> 1) & 1, ctl, a.status, 0x4b)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t v0[32], v1[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + kColDQ + 64 * db, v0);
+        tmem_ld_32x32b_x32(tmem + lane_base + kColDQ + 64 * db + 32, v1);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->dq_empty[db]);
+        float* dst = a.dq_acc + row0 * 128 + d;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) red_add_f32(dst + q * 128, __uint_as_float(v0[q]));
+#pragma unroll
+        for (int q = 0; q < 32; ++q) red_add_f32(dst + (32 + q) * 128, __uint_as_float(v1[q]));
+      }
     }
   }
-  // dK, dV -> bf16: rows key0 / key1, d columns 8 i + 2 tq, + 1
-  uint16_t* dk = a.dk + (krow0 + key0) * 128 + 2 * tq;
-  uint16_t* dv = a.dv + (krow0 + key0) * 128 + 2 * tq;
+
+  // ------------------------------------------------------------------ dK, dV epilogue
+  const bool any = g > 0;
+  if (warp == kMmaWarp) {
+    if (lane == 0) {
+      if (any && ok) mma_commit(&ctl->acc_full);
+      // every MMA issued has completed before TMEM can be released
+      mma_commit(&ctl->drain);
+      wait(&ctl->drain, 0, ctl, a.status, 0x4c, true);
+    }
+    __syncwarp();
+  } else if (warp == kTmaWarp) {
+    if (lane == 0) {  // every copy issued has landed before the CTA exits
+      if (kv_issued) wait(&ctl->kv_full, 0, ctl, a.status, 0x4d, true);
+      for (int s = 0; s < kStages; ++s)
+        if (fills[s]) wait(&ctl->ld_full[s], (fills[s] - 1) & 1, ctl, a.status, 0x4e, true);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    const int r = (warp & 3) * 32 + (int)lane;
+    const bool is_dk = warp >= 4;
+    const bool row_ok = 128 * tile + r < a.Sk;  // a lone last block-64 key block
+    uint16_t* dst = (is_dk ? a.dk : a.dv) + ((long long)bkv * a.Sk + 128 * tile + r) * 128;
+    bool have = false;
+    if (any && ok) {
+      have = wait(&ctl->acc_full, 0, ctl, a.status, 0x4f);
+      tc_fence_after();
+    }
+    if (have || !any) {
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        if (have) {
+          tmem_ld_32x32b_x32(tmem + lane_base + (is_dk ? kColDK : kColDV) + 32 * c, v);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    *reinterpret_cast<uint32_t*>(dk + 8 * i) = pack_bf16x2(dK[i][0], dK[i][1]);
-    *reinterpret_cast<uint32_t*>(dk + 8 * 128 + 8 * i) = pack_bf16x2(dK[i][2], dK[i][3]);
-    *reinterpret_cast<uint32_t*>(dv + 8 * i) = pack_bf16x2(dV[i][0], dV[i][1]);
-    *reinterpret_cast<uint32_t*>(dv + 8 * 128 + 8 * i) = pack_bf16x2(dV[i][2], dV[i][3]);
+          for (int j = 0; j < 32; ++j) v[j] = 0u;  // no query row attends this tile
+        }
+        if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            reinterpret_cast<uint4*>(dst + 32 * c)[j] = make_uint4(
+                pack_bf16x2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
+                pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+        }
+      }
+    }
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
+}  // namespace bwd
 }  // namespace vsa

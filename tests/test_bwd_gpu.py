@@ -104,3 +104,13 @@ def test_backward_larger_case():
     w = workloads.make_random_gqa(1, 8, 4, 4096, 4096, 128, 64, 16, seed=134, n_lo=16,
                                   vbs_lo=48, vbs_hi=64)
     run_and_compare(w)
+
+
+def test_backward_column_longer_than_one_list_chunk():
+    # 8 query heads share one key/value head and all 512 query blocks of each select key
+    # blocks 0 and 1: 4096 (head, query block) pairs select the first key tile, more than
+    # one 2048-entry list chunk
+    w = workloads.make_random_gqa(1, 8, 1, 512 * 64, 4 * 64, 128, 64, 2, seed=135, n_lo=2)
+    w.q2k_idx[..., 0] = 0
+    w.q2k_idx[..., 1] = 1
+    run_and_compare(w)
