@@ -166,6 +166,15 @@ __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, Ctl* ctl, u
   }
 }
 
+// The same wait by every lane of a warp that goes on to warp-collective TMEM accesses: the
+// warp proceeds only if every lane saw the phase complete, so an abort can never leave
+// part of a warp inside a .sync.aligned instruction.
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Ctl* ctl,
+                                          unsigned* status, unsigned code) {
+  const bool w = wait(bar, parity, ctl, status, code);
+  return __all_sync(0xffffffffu, w);
+}
+
 __device__ __forceinline__ void red_add_f32(float* addr, float x) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(x) : "memory");
 }
@@ -437,8 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* D_s = lse_s + 64;
         // lse and D of the step have landed (the stage is not refilled before dK of this
         // step, which waits for this warp), and S^T is in TMEM
-        if (!wait(&ctl->ld_full[st], (gg / kStages) & 1, ctl, a.status, 0x48) ||
-            !wait(&ctl->s_full, gg & 1, ctl, a.status, 0x49)) {
+        if (!wait_warp(&ctl->ld_full[st], (gg / kStages) & 1, ctl, a.status, 0x48) ||
+            !wait_warp(&ctl->s_full, gg & 1, ctl, a.status, 0x49)) {
           ok = false;
           break;
         }
@@ -467,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->p_full);
-        if (!wait(&ctl->dp_full, gg & 1, ctl, a.status, 0x4a)) {
+        if (!wait_warp(&ctl->dp_full, gg & 1, ctl, a.status, 0x4a)) {
           ok = false;
           break;
         }
@@ -507,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < n_steps; ++i) {
         const uint32_t gg = g0 + i, db = gg & 1;
         const long long row0 = entry_row0(list[i / kSubQ], i % kSubQ, a, b, hk, BLOCK);
-        if (!wait(&ctl->dq_full[db], (gg >> 1) & 1, ctl, a.status, 0x4b)) {
+        if (!wait_warp(&ctl->dq_full[db], (gg >> 1) & 1, ctl, a.status, 0x4b)) {
           ok = false;
           break;
         }
@@ -552,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint16_t* dst = (is_dk ? a.dk : a.dv) + ((long long)bkv * a.Sk + 128 * tile + r) * 128;
     bool have = false;
     if (any && ok) {
-      have = wait(&ctl->acc_full, 0, ctl, a.status, 0x4f);
+      have = wait_warp(&ctl->acc_full, 0, ctl, a.status, 0x4f);
       tc_fence_after();
     }
     if (have || !any) {
