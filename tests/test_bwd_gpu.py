@@ -114,3 +114,65 @@ def test_backward_column_longer_than_one_list_chunk():
     w.q2k_idx[..., 0] = 0
     w.q2k_idx[..., 1] = 1
     run_and_compare(w)
+
+
+def test_mid_workload_sampled_full_size():
+    # vsa_mid at full size, in the launch configuration the benchmark times.  Sampled key
+    # blocks (both blocks of a key tile, first and last tiles, several heads): the query
+    # blocks selecting a key block are the only ones feeding its dk, dv, and each of their
+    # dq rows depends only on that row's own attention, so an oracle run on just those
+    # query blocks (the block's column, one sub-problem per sample, padded with query
+    # blocks that select nothing) gives exact dk, dv for the key block and exact dq for
+    # every query block in its column.
+    w = workloads.make("vsa_mid")
+    d = torch.device("cuda:0")
+    q, k, v = (t.to(d) for t in (w.q, w.k, w.v))
+    idx, num, vbs = (torch.from_numpy(np.ascontiguousarray(x)).to(d)
+                     for x in (w.q2k_idx, w.q2k_num, w.vbs))
+    out, lse = binding.vsa_fwd_gqa(q, k, v, idx, num, vbs, block=w.block, scale=w.scale)
+    do = torch.randn(w.q.shape, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    dq, dk, dv = binding.vsa_bwd(q, k, v, out, do.to(d), lse, idx, num, vbs, block=w.block,
+                                 scale=w.scale)
+    torch.cuda.synchronize()
+    code, detail = binding.vsa_device_status()
+    assert code == binding.VSA_OK, hex(detail)
+    dq, dk, dv = (t.float().cpu().numpy().astype(np.float64) for t in (dq, dk, dv))
+
+    blk, nb, D = w.block, w.nb, w.D
+    mask = orc.lut_to_blockmask(w.q2k_idx, w.q2k_num, nb)  # [1, H, nb, nb]
+    samples = [(0, 0), (0, 255), (5, 128), (11, 63), (3, 1), (7, 200)]
+    cols = [np.nonzero(mask[0, h, :, kb])[0] for h, kb in samples]
+    nmax = max(len(c) for c in cols)
+    bits = {name: workloads.bits(t) for name, t in (("q", w.q), ("k", w.k), ("v", w.v),
+                                                    ("do", do))}
+    n = len(samples)
+    qs = np.zeros((1, n, nmax * blk, D), np.uint16)
+    dos = np.zeros_like(qs)
+    ks = np.zeros((1, n, w.S, D), np.uint16)
+    vs = np.zeros_like(ks)
+    ms = np.zeros((1, n, nmax, nb), np.int8)
+    for s, ((h, kb), col) in enumerate(zip(samples, cols)):
+        for t, qb in enumerate(col):
+            qs[0, s, t * blk:(t + 1) * blk] = bits["q"][0, h, qb * blk:(qb + 1) * blk]
+            dos[0, s, t * blk:(t + 1) * blk] = bits["do"][0, h, qb * blk:(qb + 1) * blk]
+            ms[0, s, t] = mask[0, h, qb]
+        ks[0, s] = bits["k"][0, h]
+        vs[0, s] = bits["v"][0, h]
+    rq, rk, rv = orc.masked_attention_bwd(qs, ks, vs, dos, ms, blk, w.scale, vbs=w.vbs)
+
+    got = {"dq": [], "dk": [], "dv": []}
+    ref = {"dq": [], "dk": [], "dv": []}
+    for s, ((h, kb), col) in enumerate(zip(samples, cols)):
+        keys = slice(kb * blk, (kb + 1) * blk)
+        got["dk"].append(dk[0, h, keys])
+        ref["dk"].append(rk[0, s, keys])
+        got["dv"].append(dv[0, h, keys])
+        ref["dv"].append(rv[0, s, keys])
+        for t, qb in enumerate(col):
+            got["dq"].append(dq[0, h, qb * blk:(qb + 1) * blk])
+            ref["dq"].append(rq[0, s, t * blk:(t + 1) * blk])
+    for name in ("dq", "dk", "dv"):
+        g, r = np.concatenate(got[name]), np.concatenate(ref[name])
+        e = np.abs(g - r)
+        assert e.max() <= REL_MAX * np.abs(r).max(), (name, e.max(), np.abs(r).max())
+        assert e.mean() <= REL_MEAN * np.abs(r).mean(), (name, e.mean(), np.abs(r).mean())
