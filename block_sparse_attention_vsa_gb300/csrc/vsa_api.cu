@@ -338,6 +338,10 @@ vsa_status run_map(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
   return launch_fwd<128, true>(dev, 3, q, k, v, out, p, a, s);
 }
 
+// Limits of the backward's step list (an entry packs the query block in 16 bits and the
+// query head within the key/value group in 12 bits).
+constexpr long long kBwdMaxQBlocks = 65536, kBwdMaxGroup = 4096;
+
 size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
 // Backward workspace: the 0/1 block map, D per query row, the fp32 dQ accumulator.
@@ -387,7 +391,7 @@ size_t vsa_workspace_bytes(void) { return kSchedBytes; }
 
 size_t vsa_bwd_workspace_bytes(int B, int Hq, int Sq, int Sk, int block) {
   if (B < 0 || Hq < 0 || Sq < 0 || Sk < 0 || (block != 64 && block != 128) ||
-      Sq % block != 0 || Sk % block != 0)
+      Sq % block != 0 || Sk % block != 0 || Sq / block > kBwdMaxQBlocks)
     return 0;
   return bwd_layout(B, Hq, Sq, Sk, block).total;
 }
@@ -400,6 +404,9 @@ vsa_status vsa_bwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
                    vsa_bf16* dv, void* workspace, size_t workspace_bytes,
                    vsa_stream_t stream) {
   t_last_launches = 0;
+  if ((block == 64 || block == 128) &&
+      ((long long)Sq / block > kBwdMaxQBlocks || (Hkv > 0 && Hq / Hkv > kBwdMaxGroup)))
+    return VSA_ERR_UNSUPPORTED;
   const Shape p{B, Hq, Hkv, Sq, Sk, D, block, scale};
   DeviceInfo* dev = nullptr;
   bool nothing = false;

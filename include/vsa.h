@@ -208,7 +208,8 @@ VSA_API size_t vsa_split_workspace_bytes(int B, int Hq, int Sq, int block, int n
  *                aligned, no initialisation needed (the block map, D and an fp32 dq
  *                accumulator live there).
  *   No output may overlap an input or another output.  Enqueues up to four kernels and
- *   one memset; errors as vsa_fwd_gqa.
+ *   one memset; errors as vsa_fwd_gqa, and VSA_ERR_UNSUPPORTED for more than 65536 query
+ *   blocks per head or more than 4096 query heads per key/value head.
  * Source: "FastVideo block_sparse_attn_sm100a.py", module docstring (the backward
  * consumes the forward's base-2 lse); the gradient is that of softmax attention. */
 VSA_API vsa_status vsa_bwd(const vsa_bf16 *q, const vsa_bf16 *k, const vsa_bf16 *v,

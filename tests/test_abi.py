@@ -170,6 +170,10 @@ def test_bwd_validation(lib):
     n = lib.vsa_bwd_workspace_bytes(1, 2, 256, 512, 64)
     assert n == 256 + 2 * 256 * 4 + 2 * 256 * 128 * 4
     assert lib.vsa_bwd_workspace_bytes(1, 2, 256, 500, 64) == 0
+    # the step list holds a query block in 16 bits and a head of the group in 12
+    assert _bwd(lib, Sq=64 * 65537, Hq=1) == binding.VSA_ERR_UNSUPPORTED
+    assert _bwd(lib, Hq=4097, Hkv=1) == binding.VSA_ERR_UNSUPPORTED
+    assert lib.vsa_bwd_workspace_bytes(1, 1, 64 * 65537, 512, 64) == 0
 
 
 def test_metadata_validation(lib):
