@@ -180,36 +180,36 @@ def oracle_sample(w, budget_s: float, seed: int = 0):
 
 
 def oracle_bwd_sample(w, budget_s: float):
-    """Time the oracle backward on the first query blocks of head 0 (all of its keys),
-    doubling the slice until about ``budget_s`` seconds; returns (pairs, seconds,
-    n_blocks, threads)."""
+    """Time the oracle backward on the first query blocks of the first heads (all of their
+    keys), doubling the slice until about ``budget_s`` seconds.  The oracle runs its key/value
+    heads in parallel, so the sample takes as many heads as it has threads (at most H);
+    returns (pairs, seconds, n_blocks per head, threads used, heads)."""
     import torch
     from oracle import oracle as orc
     from block_sparse_attention_vsa_gb300 import workloads
     h = orc.load()
-    threads = orc.num_threads(h)
-    hk = 0
-    kb = workloads.bits(w.k[:1, hk:hk + 1])
-    vb = workloads.bits(w.v[:1, hk:hk + 1])
+    nh = max(1, min(orc.num_threads(h), w.Hkv, w.H))
+    kb = workloads.bits(w.k[:1, :nh])
+    vb = workloads.bits(w.v[:1, :nh])
     g = torch.Generator().manual_seed(1)
     n, spent, pairs, used = 1, 0.0, 0, 0
+    vv = np.clip(w.vbs, 0, w.block)
     while n <= w.nbq:
         rows = n * w.block
-        qb = workloads.bits(w.q[:1, :1, :rows])
-        dob = workloads.bits(torch.randn((1, 1, rows, w.D), generator=g).to(torch.bfloat16))
-        idx = np.ascontiguousarray(w.q2k_idx[:1, :1, :n])
-        num = np.ascontiguousarray(w.q2k_num[:1, :1, :n])
+        qb = workloads.bits(w.q[:1, :nh, :rows])
+        dob = workloads.bits(torch.randn((1, nh, rows, w.D), generator=g).to(torch.bfloat16))
+        idx = np.ascontiguousarray(w.q2k_idx[:1, :nh, :n])
+        num = np.ascontiguousarray(w.q2k_num[:1, :nh, :n])
         t0 = time.perf_counter()
         orc.vsa_backward(qb, kb, vb, dob, idx, num, w.vbs, w.block, w.scale, h=h)
         spent = time.perf_counter() - t0
-        mask = orc.lut_to_blockmask(idx, num, w.nbk, h=h)[0, 0]
-        vv = np.clip(w.vbs, 0, w.block)
-        pairs = int(sum(int(vv[r != 0].sum()) for r in mask)) * w.block
+        mask = orc.lut_to_blockmask(idx, num, w.nbk, h=h)[0]
+        pairs = int(sum(int(vv[r != 0].sum()) for hm in mask for r in hm)) * w.block
         used = n
         if spent >= budget_s / 2 or n == w.nbq:
             break
         n = min(w.nbq, n * 2)
-    return pairs, spent, used, threads
+    return pairs, spent, used, nh, nh
 
 
 def run_reference(args, w, pairs_total, flop_per_pair):
@@ -447,11 +447,11 @@ def main():
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and bwd:
-        p, t, nblk, threads = oracle_bwd_sample(w, 15.0)
+        p, t, nblk, threads, nh = oracle_bwd_sample(w, 15.0)
         cpu = {"value": p * flop_per_pair / t / 1e12, "unit": "TFLOP/s", "cores": threads,
                "kind": "oracle",
-               "sample": f"backward of query blocks 0..{nblk - 1} of head 0 of {w.name} "
-                         f"against all its keys ({p} attended pairs, {t:.1f} s)"}
+               "sample": f"backward of query blocks 0..{nblk - 1} of heads 0..{nh - 1} of "
+                         f"{w.name} against all their keys ({p} attended pairs, {t:.1f} s)"}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not bwd:
         p, t, nblk, threads = oracle_sample(w, 15.0)
         cpu = {"value": p * flop_per_pair / t / 1e12, "unit": "TFLOP/s", "cores": threads,
