@@ -62,3 +62,19 @@ def test_reference_arm_two_ranks_prints_once():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_backward_cpu_sample_reports_the_threads_it_used():
+    # the oracle backward runs key/value heads in parallel: the sample spans as many heads
+    # as the oracle has threads (at most H), and reports that count as its cores
+    import bench
+    from block_sparse_attention_vsa_gb300 import workloads
+    from oracle import oracle as orc
+    w = workloads.make_random_vsa(1, 3, 8 * 64, 128, 64, 4, seed=5, n_lo=1)
+    pairs, seconds, n_blocks, threads, heads = bench.oracle_bwd_sample(w, 0.01)
+    assert heads == threads == min(orc.num_threads(orc.load()), 3)
+    assert n_blocks >= 1 and seconds > 0.0
+    # the attended pairs of those heads' first n_blocks query blocks
+    mask = orc.lut_to_blockmask(w.q2k_idx[:1, :heads, :n_blocks], w.q2k_num[:1, :heads, :n_blocks],
+                                w.nbk)
+    assert pairs == int(mask.sum()) * 64 * 64
