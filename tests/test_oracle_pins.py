@@ -21,6 +21,12 @@ mistake is caught.
                     on group-repeated K/V (dense, Sq != Sk), and of a masked softmax
                     written with torch.where over a token mask built by scanning the LUT
                     (tail masks, empty rows, per-head selections)
+  pin_backward_closed_forms
+                    every row attends one key -> p = 1, dS = 0: dq = dk = 0 exactly and
+                    dv_j = the sum of the dout rows (over the group) attending key j;
+                    adding one vector to every key moves each row's scores by a constant,
+                    which leaves dq, dk and dv unchanged (the D term makes each row of
+                    dS sum to zero)
   pin_gqa_cross     grouped-query heads (Hq = 3 Hkv) and Sq != Sk: dense selection equals
                     fp64 scaled_dot_product_attention on K/V repeated per group; a tiny
                     per-head sparse case equals the brute-force enumeration on the
@@ -398,8 +404,47 @@ def pin_backward(h):
     assert np.all(dq[0, 1, 16:24] == 0.0)  # the empty query block
 
 
+def pin_backward_closed_forms(h):
+    # one attended key per row: each query block selects one key block whose first key
+    # alone is valid
+    rng = np.random.default_rng(21)
+    B, Hq, Hkv, S, D, block = 1, 4, 2, 32, 8, 8
+    nb = S // block
+    q = _rand_bits((B, Hq, S, D), 931)
+    k, v = (_rand_bits((B, Hkv, S, D), 932 + i) for i in range(2))
+    do = _rand_bits((B, Hq, S, D), 935)
+    idx = rng.integers(0, nb, size=(B, Hq, nb, 1)).astype(np.int32)
+    num = np.ones((B, Hq, nb), np.int32)
+    vbs = np.ones(nb, np.int32)
+    dq, dk, dv = orc.vsa_backward(q, k, v, do, idx, num, vbs, block, 0.37, h=h)
+    assert np.all(dq == 0.0) and np.all(dk == 0.0)
+    ref = np.zeros_like(dv)
+    dof = _bits_to_f64(do)
+    g = Hq // Hkv
+    for hq in range(Hq):
+        for qb in range(nb):
+            j = int(idx[0, hq, qb, 0]) * block
+            ref[0, hq // g, j] += dof[0, hq, qb * block:(qb + 1) * block].sum(axis=0)
+    assert np.max(np.abs(dv - ref)) <= 1e-12 * max(1.0, np.abs(ref).max())
+    # keys shifted by one vector: every row's scores move by a constant
+    B, Hq, Hkv, S, D, block, max_kv = 1, 2, 1, 24, 4, 8, 3
+    nb = S // block
+    kq = rng.integers(-8, 9, size=(B, Hkv, S, D)) / 4.0      # exact in bf16, and so is
+    shift = rng.integers(-8, 9, size=D) / 4.0               # every key plus the shift
+    q = _rand_bits((B, Hq, S, D), 941)
+    v = _rand_bits((B, Hkv, S, D), 942)
+    do = _rand_bits((B, Hq, S, D), 943)
+    idx = rng.integers(0, nb, size=(B, Hq, nb, max_kv)).astype(np.int32)
+    num = rng.integers(1, max_kv + 1, size=(B, Hq, nb)).astype(np.int32)
+    vbs = rng.integers(1, block + 1, size=nb).astype(np.int32)
+    grads = [orc.vsa_backward(q, _bf16_bits(kk), v, do, idx, num, vbs, block, 0.5, h=h)
+             for kk in (kq, kq + shift)]
+    for a, b in zip(*grads):
+        assert np.max(np.abs(a - b)) <= 1e-10 * max(1.0, np.abs(a).max())
+
+
 PINS = [pin_golden, pin_dense, pin_bruteforce, pin_invariants, pin_closed_forms, pin_empty,
-        pin_encodings, pin_gqa_cross, pin_backward]
+        pin_encodings, pin_gqa_cross, pin_backward, pin_backward_closed_forms]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
