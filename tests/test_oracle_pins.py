@@ -4,7 +4,8 @@ Every pin takes an oracle handle so that tests/test_oracle_mutants.py can run th
 pins against deliberately broken copies of the oracle and show that each plausible
 mistake is caught.
 
-  pin_golden        hand-derived values (tests/golden/*.json, each with its citation)
+  pin_golden        hand-derived values (tests/golden/*.json, each with its citation;
+                    forward out and lse, and for one file the backward dq, dk, dv)
   pin_dense         all blocks selected, full blocks -> textbook softmax attention:
                     torch's scaled_dot_product_attention and logsumexp in fp64
   pin_bruteforce    tiny inputs, an independent pure-Python enumeration that decides
@@ -81,6 +82,13 @@ def pin_golden(h):
         want_lse = np.array([orc.LSE_EMPTY if x == "EMPTY" else x for x in case["lse"]])
         assert np.max(np.abs(out - want_out)) <= 1e-12, (name, out, want_out)
         assert np.max(np.abs(lse - want_lse)) <= 1e-12, (name, lse, want_lse)
+        if "dout" in case:  # a backward example
+            do = _bf16_bits(case["dout"])[None, None]
+            grads = orc.vsa_backward(q, k, v, do, idx, num, vbs, block, math.log(2.0), h=h)
+            for key, got in zip(("dq", "dk", "dv"), grads):
+                want = np.array(case[key], np.float64)
+                got = got.reshape(want.shape)
+                assert np.max(np.abs(got - want)) <= 1e-12, (name, key, got, want)
 
 
 def pin_dense(h):
