@@ -30,7 +30,7 @@ EXPORTS = ("vsa_fwd", "jenga_fwd", "vsa_workspace_bytes", "vsa_lut_to_bitmap",
            "vsa_bitmap_to_lut", "vsa_fwd_from_host", "vsa_device_status",
            "vsa_last_launch_count", "vsa_status_str", "vsa_fwd_noalloc", "vsa_fwd_gqa",
            "vsa_fwd_from_mask", "vsa_fwd_split", "vsa_split_workspace_bytes", "vsa_bwd",
-           "vsa_bwd_workspace_bytes")
+           "vsa_bwd_workspace_bytes", "vsa_set_wait_limit_ns", "vsa_set_stall_test")
 MAX_SPLITS = 64
 
 
@@ -92,6 +92,10 @@ def load(path: str = LIB_PATH):
     h.vsa_last_launch_count.argtypes = []
     h.vsa_status_str.restype = ctypes.c_char_p
     h.vsa_status_str.argtypes = [i32]
+    h.vsa_set_wait_limit_ns.restype = None
+    h.vsa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    h.vsa_set_stall_test.restype = None
+    h.vsa_set_stall_test.argtypes = [i32]
     _lib = h
     return h
 
@@ -439,3 +443,14 @@ def vsa_device_status(stream=None):
 
 def vsa_last_launch_count() -> int:
     return int(load().vsa_last_launch_count())
+
+
+def vsa_set_wait_limit_ns(ns: int) -> None:
+    """Timeout-path test hook: limit of the kernels' non-drain waits (0 = the full limit)."""
+    load().vsa_set_wait_limit_ns(int(ns))
+
+
+def vsa_set_stall_test(enable: bool) -> None:
+    """Timeout-path test hook: while on, every launch's MMA warp waits on a barrier nothing
+    completes, so the launch reports VSA_ERR_DEVICE_TIMEOUT."""
+    load().vsa_set_stall_test(1 if enable else 0)

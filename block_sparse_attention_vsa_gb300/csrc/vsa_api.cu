@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -69,6 +70,15 @@ using namespace vsa;
 namespace {
 
 thread_local int t_last_launches = 0;
+
+// Timeout-path test hooks (vsa_set_wait_limit_ns, vsa_set_stall_test), read at launch.
+std::atomic<unsigned long long> g_wait_ns{0};  // 0 = the kernels' full limit
+std::atomic<int> g_stall{0};
+
+unsigned long long launch_wait_ns(uint64_t full) {
+  const unsigned long long ns = g_wait_ns.load();
+  return ns == 0 ? full : ns;
+}
 
 struct DeviceInfo {
   bool ready = false;
@@ -208,12 +218,15 @@ FwdArgs shape_args(const Shape& p, float* lse, void* workspace, unsigned int* st
   a.n_splits = 1;
   a.part = nullptr;
   a.scale_log2 = p.scale * 1.4426950408889634f;
+  a.wait_ns = launch_wait_ns(kWaitLimitNs);
+  a.stall = g_stall.load();
   return a;
 }
 
+// One-time per-device kernel attributes (dynamic SMEM limit, registers at launch) and the
+// register-pool check; enqueues nothing.
 template <int BLOCK, bool JENGA>
-vsa_status launch_fwd(DeviceInfo* dev, int slot, const void* q, const void* k, const void* v,
-                      void* out, const Shape& p, const FwdArgs& args, cudaStream_t stream) {
+vsa_status prepare_fwd(DeviceInfo* dev, int slot) {
   auto kern = bsa_fwd_kernel<BLOCK, JENGA>;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -230,6 +243,15 @@ vsa_status launch_fwd(DeviceInfo* dev, int slot, const void* q, const void* k, c
   // The kernel moves registers between warpgroups (setmaxnreg); the launch must provide
   // the pool that re-balancing draws on, or a warpgroup would wait for registers forever.
   if ((long long)dev->regs[slot] * kThreads < (long long)kRegPoolNeeded) return VSA_ERR_UNSUPPORTED;
+  return VSA_OK;
+}
+
+template <int BLOCK, bool JENGA>
+vsa_status launch_fwd(DeviceInfo* dev, int slot, const void* q, const void* k, const void* v,
+                      void* out, const Shape& p, const FwdArgs& args, cudaStream_t stream) {
+  auto kern = bsa_fwd_kernel<BLOCK, JENGA>;
+  vsa_status st = prepare_fwd<BLOCK, JENGA>(dev, slot);
+  if (st != VSA_OK) return st;
   // With no keys at all (Sk == 0) no K/V copy is ever issued; the maps only need to encode.
   const bool keys = p.rows_k() > 0;
   const void* kp = keys ? k : q;
@@ -383,6 +405,40 @@ vsa_status launch_bwd(DeviceInfo* dev, const BwdArgs& a, const void* q, const vo
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
+// Streams and events of vsa_fwd_from_host, created once per device (no device memory).
+constexpr int kHostChunks = 8;
+struct HostPipe {
+  bool ready = false;
+  std::mutex mu;  // one host-buffer call at a time enqueues on these streams
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_join_in = nullptr;
+  cudaEvent_t ev_in[kHostChunks] = {}, ev_done[kHostChunks] = {};
+};
+HostPipe g_pipe[64];
+
+vsa_status host_pipe(HostPipe** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return VSA_ERR_CUDA;
+  HostPipe& p = g_pipe[dev];
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!p.ready) {
+    const unsigned ev = cudaEventDisableTiming;
+    if (cudaStreamCreateWithFlags(&p.s_in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p.s_out, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.ev_fork, ev) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.ev_join, ev) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.ev_join_in, ev) != cudaSuccess)
+      return VSA_ERR_CUDA;
+    for (int c = 0; c < kHostChunks; ++c)
+      if (cudaEventCreateWithFlags(&p.ev_in[c], ev) != cudaSuccess ||
+          cudaEventCreateWithFlags(&p.ev_done[c], ev) != cudaSuccess)
+        return VSA_ERR_CUDA;
+    p.ready = true;
+  }
+  *out = &p;
+  return VSA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -483,6 +539,8 @@ vsa_status vsa_bwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
   a.n_tiles = block == 64 ? (nbk + 1) / 2 : nbk;  // key tiles of 128 keys per head
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_ns = launch_wait_ns(bwd::kWaitLimitNs);
+  a.stall = g_stall.load();
   const long long n_ctas = (long long)B * Hkv * a.n_tiles;
   st = block == 64 ? launch_bwd<64>(dev, a, q, k, v, dout, rows, (long long)B * Hkv, n_ctas, s)
                    : launch_bwd<128>(dev, a, q, k, v, dout, rows, (long long)B * Hkv, n_ctas, s);
@@ -589,6 +647,7 @@ vsa_status vsa_fwd_from_host(const vsa_bf16* h_q, const vsa_bf16* h_k, const vsa
                              int32_t* d_q2k_num, int32_t* d_variable_block_sizes,
                              vsa_bf16* d_out, float* d_lse, void* workspace,
                              vsa_stream_t stream) {
+  t_last_launches = 0;
   if (B < 0 || H < 0 || S < 0 || D != VSA_HEAD_DIM || (block != 64 && block != 128) ||
       S % block != 0 || max_kv < 1)
     return (D != VSA_HEAD_DIM || (block != 64 && block != 128)) ? VSA_ERR_UNSUPPORTED
@@ -600,8 +659,6 @@ vsa_status vsa_fwd_from_host(const vsa_bf16* h_q, const vsa_bf16* h_k, const vsa
     return VSA_ERR_INVALID_ARG;
   const size_t nb = (size_t)S / block;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t tbytes = rows * D * 2;
-  const size_t lut_rows = (size_t)B * H * nb;
   // validate the device-side arguments before any copy is enqueued
   DeviceInfo* dev = nullptr;
   bool nothing = false;
@@ -610,23 +667,78 @@ vsa_status vsa_fwd_from_host(const vsa_bf16* h_q, const vsa_bf16* h_k, const vsa
       check_shape(d_q, d_k, d_v, d_out, h_lse ? d_lse : nullptr, shape, &dev, &nothing);
   if (st != VSA_OK) return st;
   if (!d_q2k_idx || !d_q2k_num || !d_variable_block_sizes) return VSA_ERR_INVALID_ARG;
-  if (cudaMemcpyAsync(d_q, h_q, tbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(d_k, h_k, tbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(d_v, h_v, tbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(d_q2k_idx, h_q2k_idx, lut_rows * max_kv * 4, cudaMemcpyHostToDevice, s) !=
-          cudaSuccess ||
-      cudaMemcpyAsync(d_q2k_num, h_q2k_num, lut_rows * 4, cudaMemcpyHostToDevice, s) !=
-          cudaSuccess ||
-      cudaMemcpyAsync(d_variable_block_sizes, h_variable_block_sizes, nb * 4,
-                      cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return VSA_ERR_CUDA;
-  st = vsa_fwd(d_q, d_k, d_v, d_q2k_idx, d_q2k_num, d_variable_block_sizes, B, H, S, D, max_kv,
-               block, scale, d_out, h_lse ? d_lse : nullptr, workspace, stream);
+  if (!workspace_ok(workspace)) return VSA_ERR_INVALID_ARG;
+  st = block == 64 ? prepare_fwd<64, false>(dev, 0) : prepare_fwd<128, false>(dev, 1);
   if (st != VSA_OK) return st;
-  if (cudaMemcpyAsync(h_out, d_out, tbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  if (status_word() == nullptr) return VSA_ERR_CUDA;
+  HostPipe* pipe = nullptr;
+  st = host_pipe(&pipe);
+  if (st != VSA_OK) return st;
+
+  // Chunks of consecutive (b, h) heads: chunk c's inputs are copied on the input stream,
+  // its forward runs on the caller's stream once they have landed, and its out / lse go
+  // back on the output stream once the forward is done, so one chunk's copies overlap
+  // another chunk's forward.  Both internal streams fork from `stream` and join it again.
+  const int bh = B * H;
+  const int n_chunks = bh < kHostChunks ? bh : kHostChunks;
+  const size_t head_bytes = (size_t)S * D * 2, lut_head = nb * (size_t)max_kv, num_head = nb;
+  std::lock_guard<std::mutex> lk(pipe->mu);
+  // on an error after the fork, still join both internal streams back into `stream`
+  auto fail = [&] {
+    cudaEventRecord(pipe->ev_join, pipe->s_out);
+    cudaEventRecord(pipe->ev_join_in, pipe->s_in);
+    cudaStreamWaitEvent(s, pipe->ev_join, 0);
+    cudaStreamWaitEvent(s, pipe->ev_join_in, 0);
     return VSA_ERR_CUDA;
-  if (h_lse && cudaMemcpyAsync(h_lse, d_lse, rows * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return VSA_ERR_CUDA;
+  };
+  if (cudaEventRecord(pipe->ev_fork, s) != cudaSuccess ||
+      cudaStreamWaitEvent(pipe->s_in, pipe->ev_fork, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(pipe->s_out, pipe->ev_fork, 0) != cudaSuccess)
+    return fail();
+  if (cudaMemcpyAsync(d_variable_block_sizes, h_variable_block_sizes, nb * 4,
+                      cudaMemcpyHostToDevice, pipe->s_in) != cudaSuccess)
+    return fail();
+  int launches = 0;
+  for (int c = 0; c < n_chunks; ++c) {
+    const int h0 = (int)((long long)bh * c / n_chunks), h1 = (int)((long long)bh * (c + 1) / n_chunks);
+    const int nh = h1 - h0;
+    const size_t t0 = (size_t)h0 * head_bytes, tb = (size_t)nh * head_bytes;
+    auto in = [&](void* dst, const void* src, size_t off, size_t n) {
+      return cudaMemcpyAsync(static_cast<uint8_t*>(dst) + off,
+                             static_cast<const uint8_t*>(src) + off, n, cudaMemcpyHostToDevice,
+                             pipe->s_in) == cudaSuccess;
+    };
+    if (!in(d_q, h_q, t0, tb) || !in(d_k, h_k, t0, tb) || !in(d_v, h_v, t0, tb) ||
+        !in(d_q2k_idx, h_q2k_idx, (size_t)h0 * lut_head * 4, (size_t)nh * lut_head * 4) ||
+        !in(d_q2k_num, h_q2k_num, (size_t)h0 * num_head * 4, (size_t)nh * num_head * 4) ||
+        cudaEventRecord(pipe->ev_in[c], pipe->s_in) != cudaSuccess ||
+        cudaStreamWaitEvent(s, pipe->ev_in[c], 0) != cudaSuccess)
+      return fail();
+    const size_t e0 = (size_t)h0 * S * D, r0 = (size_t)h0 * S;
+    st = vsa_fwd(d_q + e0, d_k + e0, d_v + e0, d_q2k_idx + (size_t)h0 * lut_head,
+                 d_q2k_num + (size_t)h0 * num_head, d_variable_block_sizes, 1, nh, S, D, max_kv,
+                 block, scale, d_out + e0, h_lse ? d_lse + r0 : nullptr, workspace, stream);
+    if (st != VSA_OK) {
+      fail();
+      return st;
+    }
+    launches += t_last_launches;
+    if (cudaEventRecord(pipe->ev_done[c], s) != cudaSuccess ||
+        cudaStreamWaitEvent(pipe->s_out, pipe->ev_done[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(reinterpret_cast<uint8_t*>(h_out) + t0,
+                        reinterpret_cast<const uint8_t*>(d_out) + t0, tb, cudaMemcpyDeviceToHost,
+                        pipe->s_out) != cudaSuccess)
+      return fail();
+    if (h_lse && cudaMemcpyAsync(h_lse + r0, d_lse + r0, (size_t)nh * S * 4,
+                                 cudaMemcpyDeviceToHost, pipe->s_out) != cudaSuccess)
+      return fail();
+  }
+  if (cudaEventRecord(pipe->ev_join, pipe->s_out) != cudaSuccess ||
+      cudaEventRecord(pipe->ev_join_in, pipe->s_in) != cudaSuccess ||
+      cudaStreamWaitEvent(s, pipe->ev_join, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(s, pipe->ev_join_in, 0) != cudaSuccess)
+    return fail();
+  t_last_launches = launches;
   return VSA_OK;
 }
 
@@ -643,6 +755,10 @@ vsa_status vsa_device_status(vsa_stream_t stream, unsigned int* detail) {
 
 int vsa_last_launch_count(void) { return t_last_launches; }
 
+void vsa_set_wait_limit_ns(unsigned long long ns) { g_wait_ns.store(ns); }
+
+void vsa_set_stall_test(int enable) { g_stall.store(enable ? 1 : 0); }
+
 }  // extern "C"
 
 // ------------------------------------------------------------------ allocation-free entry
@@ -653,10 +769,40 @@ int vsa_last_launch_count(void) { return t_last_launches; }
 static __device__ __align__(256) unsigned int g_noalloc_scratch[VSA_NOALLOC_SCRATCH_BYTES / 4];
 
 namespace {
-void* g_noalloc_addr[64] = {};  // device address of g_noalloc_scratch, per device
+// The array's device address, set up once per device context with that device current.
+// Keyed by the context's unique id: a cudaDeviceReset (or anything else that destroys and
+// recreates the context) reloads the module at a possibly different address, and the
+// next call then repeats the set-up instead of using a stale pointer.
+struct NoallocSlot {
+  unsigned long long ctx_id = 0;
+  void* addr = nullptr;
+};
+NoallocSlot g_noalloc[64];
 
-// Argument checks of vsa_fwd, repeated here so that nothing is enqueued (not even the
-// scratch reset) for a call that vsa_fwd would reject.
+bool current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Every check vsa_fwd makes before it enqueues anything -- arguments, device, kernel
+// attributes and register pool, the status word -- repeated here so that a call vsa_fwd
+// would reject enqueues nothing, not even the scratch reset.
 vsa_status noalloc_checks(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
                           const int32_t* q2k_idx, const int32_t* q2k_num,
                           const int32_t* vbs, int B, int H, int S, int D, int max_kv,
@@ -668,7 +814,9 @@ vsa_status noalloc_checks(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* 
   if (st != VSA_OK || *nothing) return st;
   if (max_kv < 1) return VSA_ERR_INVALID_ARG;
   if (!q2k_idx || !q2k_num || !vbs) return VSA_ERR_INVALID_ARG;
-  return VSA_OK;
+  st = block == 64 ? prepare_fwd<64, false>(dev, 0) : prepare_fwd<128, false>(dev, 1);
+  if (st != VSA_OK) return st;
+  return status_word() == nullptr ? VSA_ERR_CUDA : VSA_OK;
 }
 }  // namespace
 
@@ -690,15 +838,20 @@ vsa_status vsa_fwd_noalloc(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16*
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return VSA_ERR_CUDA;
   void* scratch = nullptr;
   {
-    // set-up, once per device, with that device current: the array's device address
+    // set-up, once per device (context), with that device current: the array's address
+    if (cudaSetDevice(dev) != cudaSuccess) return VSA_ERR_CUDA;
+    unsigned long long ctx = 0;
+    if (!current_context_id(&ctx)) return VSA_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_noalloc_addr[dev] == nullptr) {
+    NoallocSlot& slot = g_noalloc[dev];
+    if (slot.addr == nullptr || slot.ctx_id != ctx) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
         return VSA_ERR_CUDA;
-      g_noalloc_addr[dev] = p;
+      slot.addr = p;
+      slot.ctx_id = ctx;
     }
-    scratch = g_noalloc_addr[dev];
+    scratch = slot.addr;
   }
   // the array keeps whatever the previous call left: the scheduling counters must start
   // at zero, so clear them in stream order before the kernel

@@ -105,6 +105,8 @@ struct BwdArgs {
   int Hq, Hkv, group, Sq, Sk, nbq, nbk;
   int n_tiles;              // key tiles (of 128 keys) per key/value head
   float scale, scale_log2;
+  unsigned long long wait_ns;  // limit of the waits that are not drains (kWaitLimitNs)
+  int stall;                // test hook: the MMA warp first waits on a barrier nobody completes
 };
 
 namespace bwd {
@@ -140,6 +142,7 @@ struct Ctl {
   uint64_t p_full, ds_full;  // the 8 gradient warps wrote P^T (dS^T)
   uint64_t dq_full[2], dq_empty[2];
   uint64_t acc_full, drain;
+  uint64_t never;  // completed by nobody (the timeout test hook waits on it)
   int n_entries, go;
   uint32_t tmem_base;
   int abort_flag;
@@ -148,19 +151,21 @@ static_assert(sizeof(Ctl) <= 1024, "control block too large");
 static_assert(kOffDS % 1024 == 0 && kOffQ % 1024 == 0 && kOffDO % 1024 == 0, "swizzle atoms");
 static_assert(kSmemBytes <= 227 * 1024, "backward SMEM");
 
-// Bounded wait on an mbarrier phase (as in the forward): gives up after kWaitLimitNs,
-// recording `code` in the status word and raising the abort flag, or as soon as another
-// role has raised the flag -- unless `drain`, for copies / MMAs still in flight.
-__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, Ctl* ctl, unsigned* status,
+// Bounded wait on an mbarrier phase (as in the forward): gives up after the launch's
+// limit a.wait_ns, recording `code` in the status word and raising the abort flag, or as
+// soon as another role has raised the flag -- unless `drain`, for copies / MMAs still in
+// flight, which always runs to the full kWaitLimitNs.
+__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, Ctl* ctl, const BwdArgs& a,
                                      unsigned code, bool drain = false) {
   if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t limit = drain ? kWaitLimitNs : a.wait_ns;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (!drain && *reinterpret_cast<volatile int*>(&ctl->abort_flag)) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit) {
       *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
-      atomicCAS(status, 0u, kErrTimeout | code);
+      atomicCAS(a.status, 0u, kErrTimeout | code);
       return false;
     }
   }
@@ -170,8 +175,8 @@ __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, Ctl* ctl, u
 // warp proceeds only if every lane saw the phase complete, so an abort can never leave
 // part of a warp inside a .sync.aligned instruction.
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Ctl* ctl,
-                                          unsigned* status, unsigned code) {
-  const bool w = wait(bar, parity, ctl, status, code);
+                                          const BwdArgs& a, unsigned code) {
+  const bool w = wait(bar, parity, ctl, a, code);
   return __all_sync(0xffffffffu, w);
 }
 
@@ -231,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&ctl->acc_full, 1);
     mbar_init(&ctl->drain, 1);
+    mbar_init(&ctl->never, 1);
     ctl->abort_flag = 0;
     fence_mbar_init();
   }
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < n_steps; ++i) {
           const uint32_t gg = g0 + i, st = gg % kStages;
           if (gg >= (uint32_t)kStages &&
-              !wait(&ctl->ld_empty[st], ((gg / kStages) + 1) & 1, ctl, a.status, 0x41)) {
+              !wait(&ctl->ld_empty[st], ((gg / kStages) + 1) & 1, ctl, a, 0x41)) {
             ok = false;
             break;
           }
@@ -350,7 +356,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t v_kmaj = smem_desc_sw128(smem_addr(smem + kOffV), 16, 1024);
         const uint64_t k_mn = smem_desc_sw128(smem_addr(smem + kOffK), kKVTile / 2, 1024);
         const uint64_t ds_mn = smem_desc_sw128(smem_addr(smem + kOffDS), 8192, 1024);
-        if (g0 == 0 && !wait(&ctl->kv_full, 0, ctl, a.status, 0x42)) ok = false;
+        if (g0 == 0 && !wait(&ctl->kv_full, 0, ctl, a, 0x42)) ok = false;
+        if (ok && a.stall) {
+          // test hook: wait on a barrier no role ever completes, so the wait runs out,
+          // the status word records code 0x5f and every role unwinds
+          wait(&ctl->never, 0, ctl, a, 0x5f);
+          ok = false;
+        }
         // S^T (dP^T) of step gg: A = K (V) K-major, B = Q (dO) K-major, K = d in 8 steps
         auto issue_sd = [&](uint32_t gg, bool dp) {
           const uint32_t st = gg % kStages;
@@ -365,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         };
         if (ok) {
-          if (!wait(&ctl->ld_full[g0 % kStages], (g0 / kStages) & 1, ctl, a.status, 0x43)) {
+          if (!wait(&ctl->ld_full[g0 % kStages], (g0 / kStages) & 1, ctl, a, 0x43)) {
             ok = false;
           } else {
             tc_fence_after();
@@ -378,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < n_steps && ok; ++i) {
           const uint32_t gg = g0 + i, st = gg % kStages;
           // dV += P^T dO: A = P^T (TMEM, 64 query columns as 32 packed), B = dO MN-major
-          if (!wait(&ctl->p_full, gg & 1, ctl, a.status, 0x44)) {
+          if (!wait(&ctl->p_full, gg & 1, ctl, a, 0x44)) {
             ok = false;
             break;
           }
@@ -391,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    do_mn + ((kk * 2048) >> 4), kIdescG, (gg > 0 || kk > 0) ? 1u : 0u);
           if (i + 1 < n_steps) {  // S^T of the next step
             const uint32_t gn = gg + 1;
-            if (!wait(&ctl->ld_full[gn % kStages], (gn / kStages) & 1, ctl, a.status, 0x45)) {
+            if (!wait(&ctl->ld_full[gn % kStages], (gn / kStages) & 1, ctl, a, 0x45)) {
               ok = false;
               break;
             }
@@ -400,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&ctl->s_full);
           }
           // dK += dS^T Q
-          if (!wait(&ctl->ds_full, gg & 1, ctl, a.status, 0x46)) {
+          if (!wait(&ctl->ds_full, gg & 1, ctl, a, 0x46)) {
             ok = false;
             break;
           }
@@ -414,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&ctl->ld_empty[st]);  // Q, dO, lse, D of the stage consumed
           // dQ^T = K^T dS^T into dQ buffer gg & 1, K = keys in 8 steps
           const uint32_t db = gg & 1;
-          if (gg >= 2 && !wait(&ctl->dq_empty[db], ((gg >> 1) + 1) & 1, ctl, a.status, 0x47)) {
+          if (gg >= 2 && !wait(&ctl->dq_empty[db], ((gg >> 1) + 1) & 1, ctl, a, 0x47)) {
             ok = false;
             break;
           }
@@ -446,8 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* D_s = lse_s + 64;
         // lse and D of the step have landed (the stage is not refilled before dK of this
         // step, which waits for this warp), and S^T is in TMEM
-        if (!wait_warp(&ctl->ld_full[st], (gg / kStages) & 1, ctl, a.status, 0x48) ||
-            !wait_warp(&ctl->s_full, gg & 1, ctl, a.status, 0x49)) {
+        if (!wait_warp(&ctl->ld_full[st], (gg / kStages) & 1, ctl, a, 0x48) ||
+            !wait_warp(&ctl->s_full, gg & 1, ctl, a, 0x49)) {
           ok = false;
           break;
         }
@@ -476,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->p_full);
-        if (!wait_warp(&ctl->dp_full, gg & 1, ctl, a.status, 0x4a)) {
+        if (!wait_warp(&ctl->dp_full, gg & 1, ctl, a, 0x4a)) {
           ok = false;
           break;
         }
@@ -516,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < n_steps; ++i) {
         const uint32_t gg = g0 + i, db = gg & 1;
         const long long row0 = entry_row0(list[i / kSubQ], i % kSubQ, a, b, hk, BLOCK);
-        if (!wait_warp(&ctl->dq_full[db], (gg >> 1) & 1, ctl, a.status, 0x4b)) {
+        if (!wait_warp(&ctl->dq_full[db], (gg >> 1) & 1, ctl, a, 0x4b)) {
           ok = false;
           break;
         }
@@ -544,14 +556,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (any && ok) mma_commit(&ctl->acc_full);
       // every MMA issued has completed before TMEM can be released
       mma_commit(&ctl->drain);
-      wait(&ctl->drain, 0, ctl, a.status, 0x4c, true);
+      wait(&ctl->drain, 0, ctl, a, 0x4c, true);
     }
     __syncwarp();
   } else if (warp == kTmaWarp) {
     if (lane == 0) {  // every copy issued has landed before the CTA exits
-      if (kv_issued) wait(&ctl->kv_full, 0, ctl, a.status, 0x4d, true);
+      if (kv_issued) wait(&ctl->kv_full, 0, ctl, a, 0x4d, true);
       for (int s = 0; s < kStages; ++s)
-        if (fills[s]) wait(&ctl->ld_full[s], (fills[s] - 1) & 1, ctl, a.status, 0x4e, true);
+        if (fills[s]) wait(&ctl->ld_full[s], (fills[s] - 1) & 1, ctl, a, 0x4e, true);
     }
     __syncwarp();
   } else if (warp < 8) {
@@ -561,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint16_t* dst = (is_dk ? a.dk : a.dv) + ((long long)bkv * a.Sk + 128 * tile + r) * 128;
     bool have = false;
     if (any && ok) {
-      have = wait_warp(&ctl->acc_full, 0, ctl, a.status, 0x4f);
+      have = wait_warp(&ctl->acc_full, 0, ctl, a, 0x4f);
       tc_fence_after();
     }
     if (have || !any) {

@@ -57,9 +57,9 @@ constexpr int kStages = 4;
 constexpr int kMaxNb = 2048;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per wait
 // log2 units: the running max may lag the true one by up to 2^32 before O and l are
-// rescaled (each rescale waits for the previous PV).  P <= 2^32 is exact in range for
-// bf16; with at most 2048 * 64 keys per row, l <= 2^49 and |O| <= 2^49 max|v| stay
-// finite in fp32 for |v| < 6e23.
+// rescaled (each rescale waits for the previous PV).  P <= 2^32 is in range for bf16;
+// with at most 2048 * 128 keys per row (2048 blocks of 128), l <= 2^50 and
+// |O| <= 2^50 max|v| stay finite in fp32 for |v| < 3e23.
 constexpr float kRescaleThreshold = 32.0f;
 constexpr uint32_t kSoftmaxRegs = 216;            // per thread, softmax warpgroups
 constexpr uint32_t kOtherRegs = 56;               // per thread, TMA / MMA / list warps
@@ -101,6 +101,7 @@ struct SmemCtl {
   uint64_t stats_bar[2];
   uint64_t epi_bar[2];
   uint64_t drain;
+  uint64_t never;   // completed by nobody (the timeout test hook waits on it)
   int hdr_item[2];  // work unit (item * n_splits + split), -1 = no more work
   int hdr_n[2];     // list entries of the unit
   int hdr_off[2];   // index of the unit's first entry in the item's list
@@ -126,6 +127,8 @@ struct FwdArgs {
   int Hq, Hkv, group, Sq, Sk, nbq, nbk, max_kv, n_items, items_per_bh;
   int n_splits;            // key-tile ranges per item; n_items counts units (item, range)
   float scale_log2;
+  unsigned long long wait_ns;  // limit of the waits that are not drains (kWaitLimitNs)
+  int stall;               // test hook: the MMA warp first waits on a barrier nobody completes
 };
 
 // Split-KV partial of one unit: O [128 rows][128] fp32, unnormalised relative to the
@@ -133,23 +136,34 @@ struct FwdArgs {
 // nothing in the unit's range).
 constexpr int kPartFloats = 128 * 128 + 3 * 128;
 
-// Bounded wait on an mbarrier phase.  Gives up after kWaitLimitNs (recording `code` in
-// the device status word and raising the CTA's abort flag), or as soon as another role
-// has raised the abort flag -- unless `drain`: a wait for copies / MMAs still in flight
-// runs to its own time limit, so nothing is in flight when the CTA exits.
+// Bounded wait on an mbarrier phase.  Gives up after the launch's limit a.wait_ns
+// (recording `code` in the device status word and raising the CTA's abort flag), or as
+// soon as another role has raised the abort flag -- unless `drain`: a wait for copies /
+// MMAs still in flight always runs to the full kWaitLimitNs, so nothing is in flight
+// when the CTA exits.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, SmemCtl* ctl,
-                                         unsigned* status, unsigned code, bool drain = false) {
+                                         const FwdArgs& a, unsigned code, bool drain = false) {
   if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t limit = drain ? kWaitLimitNs : a.wait_ns;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (!drain && *reinterpret_cast<volatile int*>(&ctl->abort_flag)) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit) {
       *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
-      atomicCAS(status, 0u, kErrTimeout | code);
+      atomicCAS(a.status, 0u, kErrTimeout | code);
       return false;
     }
   }
+}
+
+// The same wait by every lane of a warp that goes on to warp-collective instructions
+// (tcgen05.ld/st .sync.aligned, shuffles, votes): the warp proceeds only if every lane saw
+// the phase complete, so giving up can never leave part of a warp behind.
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, SmemCtl* ctl,
+                                          const FwdArgs& a, unsigned code) {
+  const bool w = wait_bar(bar, parity, ctl, a, code);
+  return __all_sync(0xffffffffu, w);
 }
 
 // list entry: bits 0-15 key block, bits 16-17 row-half mask, bits 20-27 valid keys
@@ -195,7 +209,7 @@ __device__ ItemHead build_list(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, ui
     got = __shfl_sync(0xffffffffu, got, 0);
     h.item = got < (unsigned)a.n_items ? (int)got : -1;
   }
-  if (it >= 2 && !wait_bar(&ctl->list_empty[buf], ((it >> 1) + 1) & 1, ctl, a.status, 1)) {
+  if (it >= 2 && !wait_warp(&ctl->list_empty[buf], ((it >> 1) + 1) & 1, ctl, a, 1)) {
     ok = false;
     return h;
   }
@@ -357,7 +371,7 @@ __device__ void tma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, const CU
   bool ok = true;
   for (uint32_t it = 0; ok; ++it) {
     const uint32_t buf = it & 1;
-    if (!wait_bar(&ctl->list_full[buf], (it >> 1) & 1, ctl, a.status, 7)) break;
+    if (!wait_warp(&ctl->list_full[buf], (it >> 1) & 1, ctl, a, 7)) break;
     const int unit = ctl->hdr_item[buf];
     const int count = ctl->hdr_n[buf];
     if (unit < 0) break;
@@ -367,7 +381,7 @@ __device__ void tma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, const CU
     const int bh = item / a.items_per_bh;
     const int qa = (item - bh * a.items_per_bh) * C::kPairs;
     // Q (also the item's output staging buffer): free once the item two back is stored
-    if (it >= 2 && !wait_bar(&ctl->q_empty[buf], ((it >> 1) + 1) & 1, ctl, a.status, 2)) break;
+    if (it >= 2 && !wait_warp(&ctl->q_empty[buf], ((it >> 1) + 1) & 1, ctl, a, 2)) break;
     const int n_tiles = (count + C::kSub - 1) / C::kSub;
     if (n_tiles > 0) {
       // key/value head of this query head (grouped-query attention)
@@ -388,7 +402,7 @@ __device__ void tma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, const CU
           if (tt < 0 || tt >= n_tiles) continue;
           const uint32_t stage = L % kStages;
           if (L >= kStages &&
-              !wait_bar(&ctl->kv_empty[stage], ((L / kStages) + 1) & 1, ctl, a.status, 3)) {
+              !wait_warp(&ctl->kv_empty[stage], ((L / kStages) + 1) & 1, ctl, a, 3)) {
             ok = false;
             break;
           }
@@ -416,9 +430,9 @@ __device__ void tma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, const CU
   }
   // drain: every copy this warp issued has landed before the CTA can exit
   for (int s = 0; s < kStages; ++s)
-    if (fills[s]) wait_bar(&ctl->kv_full[s], (fills[s] - 1) & 1, ctl, a.status, 4, true);
+    if (fills[s]) wait_bar(&ctl->kv_full[s], (fills[s] - 1) & 1, ctl, a, 4, true);
   for (int b = 0; b < 2; ++b)
-    if (qfills[b]) wait_bar(&ctl->q_full[b], (qfills[b] - 1) & 1, ctl, a.status, 5, true);
+    if (qfills[b]) wait_bar(&ctl->q_full[b], (qfills[b] - 1) & 1, ctl, a, 5, true);
 }
 
 // ------------------------------------------------------------------------------------
@@ -437,15 +451,22 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
   uint32_t nq[2] = {0, 0};   // Q fills consumed per Q buffer
   for (uint32_t it = 0;; ++it) {
     const uint32_t buf = it & 1;
-    if (!wait_bar(&ctl->list_full[buf], (it >> 1) & 1, ctl, a.status, 10)) break;
+    if (!wait_bar(&ctl->list_full[buf], (it >> 1) & 1, ctl, a, 10)) break;
     const int item = ctl->hdr_item[buf];
     const int count = ctl->hdr_n[buf];
     mbar_arrive(&ctl->list_empty[buf]);
     if (item < 0) break;
     const int n_tiles = (count + C::kSub - 1) / C::kSub;
     if (n_tiles == 0) continue;
-    if (!wait_bar(&ctl->q_full[buf], nq[buf] & 1, ctl, a.status, 11)) break;
+    if (!wait_bar(&ctl->q_full[buf], nq[buf] & 1, ctl, a, 11)) break;
     ++nq[buf];
+    if (a.stall) {
+      // test hook: wait on a barrier no role ever completes, so the wait runs out, the
+      // status word records code 31 and every role unwinds (copies already in flight
+      // are drained by their issuers)
+      wait_bar(&ctl->never, 0, ctl, a, 31);
+      break;
+    }
     tc_fence_after();
     const uint64_t qdesc = smem_desc_sw128(smem_addr(smem + kOffQ + buf * kTileBytes), 16, 1024);
     bool first[2] = {true, true};  // next PV half w is the item's first into O_w
@@ -453,7 +474,7 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
     for (int t = 0; t <= n_tiles && ok; ++t) {
       if (t < n_tiles) {  // S = Q K_t^T into S buffer (g + t) & 1
         const uint32_t stage = L % kStages;
-        if (!wait_bar(&ctl->kv_full[stage], (L / kStages) & 1, ctl, a.status, 12)) {
+        if (!wait_bar(&ctl->kv_full[stage], (L / kStages) & 1, ctl, a, 12)) {
           ok = false;
           break;
         }
@@ -476,12 +497,12 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
       if (t >= 1) {  // O_w += P V for the previous tile, one key half per warpgroup
         const int tp = t - 1;
         if (tp == 0 && ne_items >= 1 &&
-            !wait_bar(&ctl->o_empty, (ne_items - 1) & 1, ctl, a.status, 13)) {
+            !wait_bar(&ctl->o_empty, (ne_items - 1) & 1, ctl, a, 13)) {
           ok = false;
           break;
         }
         const uint32_t stage = L % kStages;
-        if (!wait_bar(&ctl->kv_full[stage], (L / kStages) & 1, ctl, a.status, 15)) {
+        if (!wait_bar(&ctl->kv_full[stage], (L / kStages) & 1, ctl, a, 15)) {
           ok = false;
           break;
         }
@@ -491,7 +512,7 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
             smem_desc_sw128(smem_addr(smem + kOffKV + stage * kTileBytes), kTileBytes / 2, 1024);
         const uint32_t pb = (g + tp) & 1;
         const uint32_t tS = tmem + kColS + pb * 128;
-        if (!wait_bar(&ctl->p_full[pb], pc[pb] & 1, ctl, a.status, 14)) {
+        if (!wait_bar(&ctl->p_full[pb], pc[pb] & 1, ctl, a, 14)) {
           ok = false;
           break;
         }
@@ -519,7 +540,7 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
   }
   // every MMA issued has completed before TMEM can be released
   mma_commit(&ctl->drain);
-  wait_bar(&ctl->drain, 0, ctl, a.status, 16, true);
+  wait_bar(&ctl->drain, 0, ctl, a, 16, true);
 }
 
 // ------------------------------------------------------------------------------------
@@ -606,7 +627,7 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
   uint32_t ne_items = 0;
   for (uint32_t it = 0;; ++it) {
     const uint32_t buf = it & 1;
-    if (!wait_bar(&ctl->list_full[buf], (it >> 1) & 1, ctl, a.status, 20)) break;
+    if (!wait_warp(&ctl->list_full[buf], (it >> 1) & 1, ctl, a, 20)) break;
     const int unit = ctl->hdr_item[buf];
     const int count = ctl->hdr_n[buf];
     if (unit < 0) break;
@@ -635,7 +656,7 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
       const uint32_t sb = g & 1;
       // ring order K0, K1, V0, K2, V1, ...: K(t) sits at t ? 2t - 1 : 0, V(t) at 2t + 2
       const uint32_t kpos = ring + (t ? 2u * t - 1u : 0u);
-      if (!wait_bar(&ctl->kv_empty[kpos % kStages], (kpos / kStages) & 1, ctl, a.status, 21)) {
+      if (!wait_warp(&ctl->kv_empty[kpos % kStages], (kpos / kStages) & 1, ctl, a, 21)) {
         ok = false;
         break;
       }
@@ -657,7 +678,7 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
       // has completed (TMEM access is warp-collective, hence the vote).
       if (__any_sync(0xffffffffu, alpha != 1.0f) && started) {
         const uint32_t vpos = ring + 2u * t;  // V(t - 1)
-        if (!wait_bar(&ctl->kv_empty[vpos % kStages], (vpos / kStages) & 1, ctl, a.status, 25)) {
+        if (!wait_warp(&ctl->kv_empty[vpos % kStages], (vpos / kStages) & 1, ctl, a, 25)) {
           ok = false;
           break;
         }
@@ -688,10 +709,10 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->stats_bar[buf]);
     if (n_tiles > 0) {
-      if (!wait_bar(&ctl->o_full, ne_items & 1, ctl, a.status, 22)) break;
+      if (!wait_warp(&ctl->o_full, ne_items & 1, ctl, a, 22)) break;
       tc_fence_after();
     }
-    if (!wait_bar(&ctl->stats_bar[buf], (it >> 1) & 1, ctl, a.status, 23)) break;
+    if (!wait_warp(&ctl->stats_bar[buf], (it >> 1) & 1, ctl, a, 23)) break;
     float m[2], le[2], lr[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -771,8 +792,10 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
       mbar_arrive(&ctl->epi_bar[w]);
     }
     if (n_tiles > 0) ++ne_items;
+    // the leader waits alone; the vote keeps the decision to stop warp-uniform
+    const bool stored = !leader || wait_bar(&ctl->epi_bar[w], it & 1, ctl, a, 24);
+    if (!__all_sync(0xffffffffu, stored)) break;
     if (leader) {
-      if (!wait_bar(&ctl->epi_bar[w], it & 1, ctl, a.status, 24)) break;
       if (!split) {
         tma_store_3d(to, qs, w * 64, qa * BLOCK, bh);  // rows past Sq are not written
         bulk_commit_group();
@@ -812,6 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->o_full, 1);
     mbar_init(&ctl->o_empty, 8);
     mbar_init(&ctl->drain, 1);
+    mbar_init(&ctl->never, 1);
     ctl->abort_flag = 0;
     fence_mbar_init();
   }

@@ -238,15 +238,19 @@ VSA_API size_t vsa_workspace_bytes(void);
  * nothing and calls no allocating routine: its dynamic-schedule scratch is a static
  * device array of VSA_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU
  * that loads the library keeps until the process exits.
- *   - The first call on a device looks up that array's device address (with the device
- *     current) and caches it; make that first call before any stream capture begins.
- *   - Every call on a device shares the array.  Each call clears the scheduling counters
- *     in stream order before its kernel, so calls on one stream are safe; calls that
- *     overlap on the GPU (different streams without ordering between them) race on the
- *     counters and must not be issued.
+ *   - The first call on a device (with that device current) looks up the array's
+ *     device address and caches it for the device's current context; a later call in
+ *     a new context (after cudaDeviceReset, say) looks it up again.  Make the first
+ *     call on a device before any stream capture begins.
+ *   - Every call on a device shares the array, which keeps what the last call left.
+ *     Each call clears the scheduling counters in stream order before its kernel, so
+ *     calls on one stream are safe; calls that overlap on the GPU (different streams
+ *     without ordering between them) race on the counters and must not be issued.
  *   - A call whose scratch need exceeds VSA_NOALLOC_SCRATCH_BYTES returns
- *     VSA_ERR_UNSUPPORTED; other errors are those of vsa_fwd, checked before anything
- *     is enqueued. */
+ *     VSA_ERR_UNSUPPORTED.  Argument errors and unsupported configurations are those
+ *     of vsa_fwd and are reported before anything is enqueued; a VSA_ERR_CUDA from a
+ *     failed launch can come after the scratch reset was enqueued (harmless: the
+ *     scratch is left zero). */
 VSA_API vsa_status vsa_fwd_noalloc(const vsa_bf16 *q, const vsa_bf16 *k, const vsa_bf16 *v,
                                    const int32_t *q2k_idx, const int32_t *q2k_num,
                                    const int32_t *variable_block_sizes, int B, int H, int S,
@@ -272,10 +276,18 @@ VSA_API vsa_status vsa_bitmap_to_lut(const int8_t *bitmap, int rows, int nb, int
 
 /* vsa_fwd with HOST buffers: copies q, k, v, q2k_idx, q2k_num, variable_block_sizes
  * from host memory into the caller's device buffers (the d_* arguments, same shapes as
- * vsa_fwd), runs vsa_fwd, and copies out (and lse, if h_lse is not NULL) back to host
- * memory, all enqueued on `stream`.  The caller synchronises the stream before reading
- * h_out / h_lse.  Host buffers should be pinned (page-locked) for the copies to be
- * asynchronous.  d_lse may be NULL only if h_lse is NULL. */
+ * vsa_fwd), runs the forward, and copies out (and lse, if h_lse is not NULL) back to host
+ * memory.  The work is split into up to 8 chunks of consecutive (b, h) heads: a chunk's
+ * inputs go over on an input stream, its forward runs on `stream` as soon as they have
+ * landed, and its outputs come back on an output stream, so copies of one chunk overlap
+ * the forward of another.  The two internal streams (and their events) are created once
+ * per device on first use -- no device memory -- and fork from `stream` at the start of
+ * the call and join it at the end: everything is ordered after earlier work on `stream`,
+ * and later work on `stream` (or a synchronisation of it) sees the whole call complete.
+ * The caller synchronises `stream` before reading h_out / h_lse.  Host buffers should
+ * be pinned (page-locked) for the copies to be asynchronous.  d_lse may be NULL only if
+ * h_lse is NULL.  Calls from several host threads are serialised on an internal lock.
+ * Argument errors are reported before anything is enqueued. */
 VSA_API vsa_status vsa_fwd_from_host(const vsa_bf16 *h_q, const vsa_bf16 *h_k, const vsa_bf16 *h_v,
                              const int32_t *h_q2k_idx, const int32_t *h_q2k_num,
                              const int32_t *h_variable_block_sizes, int B, int H, int S,
@@ -293,6 +305,21 @@ VSA_API vsa_status vsa_device_status(vsa_stream_t stream, unsigned int *detail);
 /* Number of kernel launches the most recent successful forward call on this thread
  * enqueued (for accounting in benchmarks). */
 VSA_API int vsa_last_launch_count(void);
+
+/* Test hooks for the timeout path (failure detection without a GPU fault).  Both are
+ * process-wide settings read when a forward or backward kernel is launched; they change
+ * no result of a launch that completes.  (The pages have no counterpart.)
+ *   vsa_set_wait_limit_ns(ns): the limit of every internal wait that is not a drain
+ *     (a drain waits for the kernel's own copies and MMAs in flight and always keeps the
+ *     full limit of about one second, so nothing is in flight when a CTA exits).
+ *     0 restores the full limit.  A short limit makes waits run out on ordinary work.
+ *   vsa_set_stall_test(enable): while nonzero, the MMA warp of every CTA first waits on
+ *     a barrier that nothing ever completes; that wait runs out after the limit above,
+ *     records its code in the device status word (forward 0x11f, backward 0x15f), and
+ *     every role of the CTA returns.  The launch's outputs are then undefined and
+ *     vsa_device_status() reports VSA_ERR_DEVICE_TIMEOUT. */
+VSA_API void vsa_set_wait_limit_ns(unsigned long long ns);
+VSA_API void vsa_set_stall_test(int enable);
 
 /* Static text for a status code. */
 VSA_API const char *vsa_status_str(vsa_status s);

@@ -218,6 +218,47 @@ def test_from_host_buffers():
     assert torch.equal(h_out, ref_out.cpu()) and torch.equal(h_lse, ref_lse.cpu())
 
 
+@pytest.mark.parametrize("block,B,H,with_lse,dynamic", [(64, 2, 5, True, False),
+                                                          (128, 1, 3, False, True),
+                                                          (64, 1, 11, True, True)])
+def test_from_host_chunks_on_a_side_stream(block, B, H, with_lse, dynamic):
+    """The host-buffer entry splits the heads into up to 8 chunks (uneven ones included)
+    whose copies overlap other chunks' forwards on internal streams forked from the caller's
+    stream; the result equals vsa_fwd's bit for bit and the oracle's within tolerance, and
+    work enqueued on the caller's stream afterwards sees the copies complete."""
+    w = small(block, 23 + H, B=B, H=H)
+    dev = to_dev(w)
+    ref_out, ref_lse = run_gpu(w, dev)
+    compare(w, ref_out, ref_lse)
+    h = dict(q=w.q.pin_memory(), k=w.k.pin_memory(), v=w.v.pin_memory(),
+             idx=torch.from_numpy(w.q2k_idx).pin_memory(),
+             num=torch.from_numpy(w.q2k_num).pin_memory(),
+             vbs=torch.from_numpy(w.vbs).pin_memory())
+    h_out = torch.full_like(w.q, float("nan")).pin_memory()
+    h_lse = torch.full((w.B, w.H, w.S), float("nan"), dtype=torch.float32).pin_memory()
+    bufs = {kk: torch.zeros_like(t) for kk, t in dev.items()}
+    bufs["out"] = torch.empty_like(dev["q"])
+    bufs["lse"] = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    ws = binding.new_workspace(dev["q"].device) if dynamic else None
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        binding.vsa_fwd_from_host(h["q"], h["k"], h["v"], h["idx"], h["num"], h["vbs"], w.block,
+                                  w.scale, h_out, h_lse if with_lse else None, bufs,
+                                  workspace=ws, stream=side)
+        # enqueued after the call on the same stream: must see every chunk's copy done
+        probe = bufs["out"].float().sum()
+    side.synchronize()
+    assert binding.vsa_last_launch_count() == min(8, B * H)
+    assert torch.equal(h_out, ref_out.cpu())
+    assert torch.equal(bufs["q"], dev["q"]) and torch.equal(bufs["idx"], dev["idx"])
+    assert probe.item() == ref_out.float().sum().item()
+    if with_lse:
+        assert torch.equal(h_lse, ref_lse.cpu())
+    code, detail = binding.vsa_device_status()
+    assert code == binding.VSA_OK, hex(detail)
+
+
 # ------------------------------------------------------------- metadata conversions
 def test_lut_to_bitmap_bit_exact():
     rng = np.random.default_rng(3)
