@@ -116,15 +116,14 @@ def test_backward_column_longer_than_one_list_chunk():
     run_and_compare(w)
 
 
-def test_mid_workload_sampled_full_size():
-    # vsa_mid at full size, in the launch configuration the benchmark times.  Sampled key
-    # blocks (both blocks of a key tile, first and last tiles, several heads): the query
-    # blocks selecting a key block are the only ones feeding its dk, dv, and each of their
-    # dq rows depends only on that row's own attention, so an oracle run on just those
-    # query blocks (the block's column, one sub-problem per sample, padded with query
-    # blocks that select nothing) gives exact dk, dv for the key block and exact dq for
-    # every query block in its column.
-    w = workloads.make("vsa_mid")
+def _sampled_full_size(w, samples):
+    """The backward of workload ``w`` at full size, in the launch configuration the
+    benchmark times, checked on sampled key blocks ``samples`` = [(b, h, kb)].  The query
+    blocks selecting a key block are the only ones feeding its dk, dv, and each of their dq
+    rows depends only on that row's own attention (over every key its query block selects),
+    so an oracle run on just those query blocks with the head's full keys (one sub-problem
+    per sample, padded with query blocks that select nothing) gives exact dk, dv for the
+    key block and exact dq for every query block in its column."""
     d = torch.device("cuda:0")
     q, k, v = (t.to(d) for t in (w.q, w.k, w.v))
     idx, num, vbs = (torch.from_numpy(np.ascontiguousarray(x)).to(d)
@@ -137,11 +136,12 @@ def test_mid_workload_sampled_full_size():
     code, detail = binding.vsa_device_status()
     assert code == binding.VSA_OK, hex(detail)
     dq, dk, dv = (t.float().cpu().numpy().astype(np.float64) for t in (dq, dk, dv))
+    del q, k, v, idx, num, vbs, out, lse
 
     blk, nb, D = w.block, w.nb, w.D
-    mask = orc.lut_to_blockmask(w.q2k_idx, w.q2k_num, nb)  # [1, H, nb, nb]
-    samples = [(0, 0), (0, 255), (5, 128), (11, 63), (3, 1), (7, 200)]
-    cols = [np.nonzero(mask[0, h, :, kb])[0] for h, kb in samples]
+    mask = orc.lut_to_blockmask(w.q2k_idx, w.q2k_num, nb)  # [B, H, nb, nb]
+    cols = [np.nonzero(mask[b, h, :, kb])[0] for b, h, kb in samples]
+    assert all(len(c) > 0 for c in cols), "a sampled key block no query block selects"
     nmax = max(len(c) for c in cols)
     bits = {name: workloads.bits(t) for name, t in (("q", w.q), ("k", w.k), ("v", w.v),
                                                     ("do", do))}
@@ -151,28 +151,42 @@ def test_mid_workload_sampled_full_size():
     ks = np.zeros((1, n, w.S, D), np.uint16)
     vs = np.zeros_like(ks)
     ms = np.zeros((1, n, nmax, nb), np.int8)
-    for s, ((h, kb), col) in enumerate(zip(samples, cols)):
+    for s, ((b, h, kb), col) in enumerate(zip(samples, cols)):
         for t, qb in enumerate(col):
-            qs[0, s, t * blk:(t + 1) * blk] = bits["q"][0, h, qb * blk:(qb + 1) * blk]
-            dos[0, s, t * blk:(t + 1) * blk] = bits["do"][0, h, qb * blk:(qb + 1) * blk]
-            ms[0, s, t] = mask[0, h, qb]
-        ks[0, s] = bits["k"][0, h]
-        vs[0, s] = bits["v"][0, h]
+            qs[0, s, t * blk:(t + 1) * blk] = bits["q"][b, h, qb * blk:(qb + 1) * blk]
+            dos[0, s, t * blk:(t + 1) * blk] = bits["do"][b, h, qb * blk:(qb + 1) * blk]
+            ms[0, s, t] = mask[b, h, qb]
+        ks[0, s] = bits["k"][b, h]
+        vs[0, s] = bits["v"][b, h]
     rq, rk, rv = orc.masked_attention_bwd(qs, ks, vs, dos, ms, blk, w.scale, vbs=w.vbs)
 
     got = {"dq": [], "dk": [], "dv": []}
     ref = {"dq": [], "dk": [], "dv": []}
-    for s, ((h, kb), col) in enumerate(zip(samples, cols)):
+    for s, ((b, h, kb), col) in enumerate(zip(samples, cols)):
         keys = slice(kb * blk, (kb + 1) * blk)
-        got["dk"].append(dk[0, h, keys])
+        got["dk"].append(dk[b, h, keys])
         ref["dk"].append(rk[0, s, keys])
-        got["dv"].append(dv[0, h, keys])
+        got["dv"].append(dv[b, h, keys])
         ref["dv"].append(rv[0, s, keys])
         for t, qb in enumerate(col):
-            got["dq"].append(dq[0, h, qb * blk:(qb + 1) * blk])
+            got["dq"].append(dq[b, h, qb * blk:(qb + 1) * blk])
             ref["dq"].append(rq[0, s, t * blk:(t + 1) * blk])
     for name in ("dq", "dk", "dv"):
         g, r = np.concatenate(got[name]), np.concatenate(ref[name])
         e = np.abs(g - r)
         assert e.max() <= REL_MAX * np.abs(r).max(), (name, e.max(), np.abs(r).max())
         assert e.mean() <= REL_MEAN * np.abs(r).mean(), (name, e.mean(), np.abs(r).mean())
+
+
+def test_mid_workload_sampled_full_size():
+    # vsa_mid: both blocks of a key tile, the first and last tiles, several heads
+    w = workloads.make("vsa_mid")
+    _sampled_full_size(w, [(0, 0, 0), (0, 0, 255), (0, 5, 128), (0, 11, 63), (0, 3, 1),
+                           (0, 7, 200)])
+
+
+def test_blk128_workload_sampled_full_size():
+    # vsa_blk128 (two batches, 24 heads, block 128, tail masks 96..128): the first and
+    # last key blocks, both batches, several heads
+    w = workloads.make("vsa_blk128")
+    _sampled_full_size(w, [(0, 0, 0), (1, 23, 255), (0, 17, 128), (1, 4, 31), (1, 9, 200)])
