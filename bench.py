@@ -271,6 +271,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"],
                     help="bwd times vsa_bwd (dq, dk, dv) on the workload instead")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="time only the first N heads of the workload (a smaller case of the "
+                         "same per-head structure, for profiler captures)")
     args = ap.parse_args()
 
     import torch
@@ -278,6 +281,8 @@ def main():
 
     ws, rank, local = dist_env()
     w = workloads.make(args.workload, seed=0)
+    if args.heads:
+        w = workloads.first_heads(w, args.heads)
     pairs = attended_pairs(w)
     bwd = args.pass_ == "bwd"
     if bwd and w.kind != "vsa":

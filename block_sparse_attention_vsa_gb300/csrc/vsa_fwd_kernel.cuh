@@ -23,8 +23,9 @@
 //               entries can never cause a duplicate or an out-of-bounds copy.  Block-64
 //               lists put blocks only one query block selects in alternating pairs first
 //               (see build_list).  Lists are double-buffered.
-//   warp 8      TMA: Q (double-buffered across items) and ONLY the selected K/V blocks
-//               into a 4-stage ring, in the order the MMA warp consumes them.
+//   warp 8      TMA (one thread): Q (double-buffered across items) and ONLY the
+//               selected K/V blocks into a 4-stage ring, in the order the MMA warp
+//               consumes them.
 //   warp 9      MMA issuer (one thread): S_g = Q K_g^T into TMEM S buffer g%2 (g counts
 //               key tiles across items), then, per key half w, O_w += P_g[:, 64w:64w+64]
 //               V_g[64w:64w+64, :] with P read from TMEM.  Issue order QK0, QK1, PV0,
@@ -42,7 +43,9 @@
 // TMEM (512 columns): S0, S1 at columns 0, 128 (warpgroup w reads S columns 64w..64w+63
 // and writes its bf16 P over the first 32 of them); O0, O1 at 256, 384.
 // Every mbarrier wait is bounded; a wait that runs out records a code in the device
-// status word, raises the CTA's abort flag and every role returns.
+// status word, raises the CTA's abort flag and every role returns.  Waits that a whole
+// warp goes on from into warp-collective instructions (the list and softmax warps) are
+// warp votes, so a warp never splits; the TMA and MMA roles run on one thread each.
 #pragma once
 
 #include <cuda.h>
@@ -361,17 +364,16 @@ __device__ void list_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a) {
 template <int BLOCK, bool JENGA>
 __device__ void tma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, const CUtensorMap* tq,
                          const CUtensorMap* tk, const CUtensorMap* tv) {
+  // one thread issues every copy; its waits are its own (no warp collective follows them)
   using C = Cfg<BLOCK>;
-  const uint32_t lane = lane_id();
   const uint64_t pol_kv = policy_evict_last();
   const uint64_t pol_q = policy_evict_first();
   uint32_t L = 0;                            // K/V tiles loaded so far (ring position)
-  uint32_t fills[kStages] = {0, 0, 0, 0};    // copies issued per ring stage
-  uint32_t qfills[2] = {0, 0};               // Q copies issued per Q buffer
+  uint32_t qf0 = 0, qf1 = 0;                 // Q copies issued per Q buffer
   bool ok = true;
   for (uint32_t it = 0; ok; ++it) {
     const uint32_t buf = it & 1;
-    if (!wait_warp(&ctl->list_full[buf], (it >> 1) & 1, ctl, a, 7)) break;
+    if (!wait_bar(&ctl->list_full[buf], (it >> 1) & 1, ctl, a, 7)) break;
     const int unit = ctl->hdr_item[buf];
     const int count = ctl->hdr_n[buf];
     if (unit < 0) break;
@@ -381,19 +383,17 @@ __device__ void tma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, const CU
     const int bh = item / a.items_per_bh;
     const int qa = (item - bh * a.items_per_bh) * C::kPairs;
     // Q (also the item's output staging buffer): free once the item two back is stored
-    if (it >= 2 && !wait_warp(&ctl->q_empty[buf], ((it >> 1) + 1) & 1, ctl, a, 2)) break;
+    if (it >= 2 && !wait_bar(&ctl->q_empty[buf], ((it >> 1) + 1) & 1, ctl, a, 2)) break;
     const int n_tiles = (count + C::kSub - 1) / C::kSub;
     if (n_tiles > 0) {
       // key/value head of this query head (grouped-query attention)
       const int kvh = (bh / a.Hq) * a.Hkv + (bh % a.Hq) / a.group;
       uint8_t* qs = smem + kOffQ + buf * kTileBytes;
-      if (lane == 0) {
-        // 128 query rows of head bh; rows past Sq (a lone last block) read as zeros
-        mbar_arrive_expect_tx(&ctl->q_full[buf], kTileBytes);
-        tma_load_3d_hint(qs, tq, &ctl->q_full[buf], 0, qa * BLOCK, bh, pol_q);
-        tma_load_3d_hint(qs + kTileBytes / 2, tq, &ctl->q_full[buf], 64, qa * BLOCK, bh, pol_q);
-      }
-      ++qfills[buf];
+      // 128 query rows of head bh; rows past Sq (a lone last block) read as zeros
+      mbar_arrive_expect_tx(&ctl->q_full[buf], kTileBytes);
+      tma_load_3d_hint(qs, tq, &ctl->q_full[buf], 0, qa * BLOCK, bh, pol_q);
+      tma_load_3d_hint(qs + kTileBytes / 2, tq, &ctl->q_full[buf], 64, qa * BLOCK, bh, pol_q);
+      if (buf) ++qf1; else ++qf0;
       // K/V tiles in the order the MMA warp consumes them: K0, K1, V0, K2, V1, ...
       for (int t = 0; t <= n_tiles && ok; ++t) {
 #pragma unroll
@@ -402,7 +402,7 @@ __device__ void tma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, const CU
           if (tt < 0 || tt >= n_tiles) continue;
           const uint32_t stage = L % kStages;
           if (L >= kStages &&
-              !wait_warp(&ctl->kv_empty[stage], ((L / kStages) + 1) & 1, ctl, a, 3)) {
+              !wait_bar(&ctl->kv_empty[stage], ((L / kStages) + 1) & 1, ctl, a, 3)) {
             ok = false;
             break;
           }
@@ -410,29 +410,28 @@ __device__ void tma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, const CU
           uint8_t* dst = smem + kOffKV + stage * kTileBytes;
           const int e0 = tt * C::kSub;
           const int ne = (count - e0) < C::kSub ? (count - e0) : C::kSub;
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&ctl->kv_full[stage], (uint32_t)ne * BLOCK * 128 * 2);
-            for (int e = 0; e < ne; ++e) {
-              const int krow = kvh * a.Sk + (int)(list[e0 + e] & 0xFFFFu) * BLOCK;
-              // d-halves are separate [128 rows][64] sub-tiles; block e fills rows e*BLOCK..
-              tma_load_2d_hint(dst + e * BLOCK * 128, map, &ctl->kv_full[stage], 0, krow, pol_kv);
-              tma_load_2d_hint(dst + kTileBytes / 2 + e * BLOCK * 128, map, &ctl->kv_full[stage],
-                               64, krow, pol_kv);
-            }
+          mbar_arrive_expect_tx(&ctl->kv_full[stage], (uint32_t)ne * BLOCK * 128 * 2);
+          for (int e = 0; e < ne; ++e) {
+            const int krow = kvh * a.Sk + (int)(list[e0 + e] & 0xFFFFu) * BLOCK;
+            // d-halves are separate [128 rows][64] sub-tiles; block e fills rows e*BLOCK..
+            tma_load_2d_hint(dst + e * BLOCK * 128, map, &ctl->kv_full[stage], 0, krow, pol_kv);
+            tma_load_2d_hint(dst + kTileBytes / 2 + e * BLOCK * 128, map, &ctl->kv_full[stage],
+                             64, krow, pol_kv);
           }
-          ++fills[stage];
           ++L;
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl->list_empty[buf]);  // done reading this item's list
+    mbar_arrive(&ctl->list_empty[buf]);  // done reading this item's list
   }
-  // drain: every copy this warp issued has landed before the CTA can exit
-  for (int s = 0; s < kStages; ++s)
-    if (fills[s]) wait_bar(&ctl->kv_full[s], (fills[s] - 1) & 1, ctl, a, 4, true);
-  for (int b = 0; b < 2; ++b)
-    if (qfills[b]) wait_bar(&ctl->q_full[b], (qfills[b] - 1) & 1, ctl, a, 5, true);
+  // drain: every copy this thread issued has landed before the CTA can exit (ring
+  // positions 0..L-1 went to stage position % kStages)
+  for (uint32_t s = 0; s < (uint32_t)kStages; ++s) {
+    const uint32_t fills = L > s ? (L - s + kStages - 1) / kStages : 0;
+    if (fills) wait_bar(&ctl->kv_full[s], (fills - 1) & 1, ctl, a, 4, true);
+  }
+  if (qf0) wait_bar(&ctl->q_full[0], (qf0 - 1) & 1, ctl, a, 5, true);
+  if (qf1) wait_bar(&ctl->q_full[1], (qf1 - 1) & 1, ctl, a, 5, true);
 }
 
 // ------------------------------------------------------------------------------------
@@ -445,10 +444,10 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
   constexpr uint32_t kIdescS64 = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);
   uint32_t L = 0;            // ring position
-  uint32_t g = 0;            // key tiles issued so far, across items (S buffer g & 1)
-  uint32_t pc[2] = {0, 0};   // P phases per S buffer
+  uint32_t g = 0;            // key tiles issued so far, across items (S buffer g & 1; the
+                             // tile's P phase on that buffer is g >> 1)
   uint32_t ne_items = 0;     // non-empty items so far (O phases)
-  uint32_t nq[2] = {0, 0};   // Q fills consumed per Q buffer
+  uint32_t nq0 = 0, nq1 = 0; // Q fills consumed per Q buffer (scalars: no indexed array)
   for (uint32_t it = 0;; ++it) {
     const uint32_t buf = it & 1;
     if (!wait_bar(&ctl->list_full[buf], (it >> 1) & 1, ctl, a, 10)) break;
@@ -458,8 +457,8 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
     if (item < 0) break;
     const int n_tiles = (count + C::kSub - 1) / C::kSub;
     if (n_tiles == 0) continue;
-    if (!wait_bar(&ctl->q_full[buf], nq[buf] & 1, ctl, a, 11)) break;
-    ++nq[buf];
+    if (!wait_bar(&ctl->q_full[buf], (buf ? nq1 : nq0) & 1, ctl, a, 11)) break;
+    if (buf) ++nq1; else ++nq0;
     if (a.stall) {
       // test hook: wait on a barrier no role ever completes, so the wait runs out, the
       // status word records code 31 and every role unwinds (copies already in flight
@@ -512,11 +511,10 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
             smem_desc_sw128(smem_addr(smem + kOffKV + stage * kTileBytes), kTileBytes / 2, 1024);
         const uint32_t pb = (g + tp) & 1;
         const uint32_t tS = tmem + kColS + pb * 128;
-        if (!wait_bar(&ctl->p_full[pb], pc[pb] & 1, ctl, a, 14)) {
+        if (!wait_bar(&ctl->p_full[pb], ((g + tp) >> 1) & 1, ctl, a, 14)) {
           ok = false;
           break;
         }
-        ++pc[pb];
         tc_fence_after();
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
@@ -865,7 +863,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     regs_decrease<kOtherRegs>();
     if (warp == 8) {
-      tma_role<BLOCK, JENGA>(smem, ctl, a, &tq, &tk, &tv);
+      if (lane_id() == 0) tma_role<BLOCK, JENGA>(smem, ctl, a, &tq, &tk, &tv);
+      __syncwarp();
     } else if (warp == 10) {
       list_role<BLOCK, JENGA>(smem, ctl, a);
     } else if (warp == 9) {

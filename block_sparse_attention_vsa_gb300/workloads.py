@@ -313,6 +313,26 @@ def make_random_gqa(B, Hq, Hkv, Sq, Sk, D, block, max_kv, seed, n_lo=0, n_hi=Non
     return w
 
 
+def first_heads(w: Workload, n: int) -> Workload:
+    """The same workload restricted to its first ``n`` query heads (and their key/value
+    heads): every per-head structure is unchanged, only the head count shrinks."""
+    n = max(1, min(n, w.H))
+    group = w.H // w.Hkv
+    nkv = max(1, n // group)
+    out = Workload(f"{w.name}_h{n}", w.kind, w.B, n, w.S, w.D, w.block, w.scale,
+                   w.q[:, :n].contiguous(), w.k[:, :nkv].contiguous(),
+                   w.v[:, :nkv].contiguous(), bitmap=w.bitmap, extra=dict(w.extra),
+                   Hkv=nkv, Sk=w.Sk)
+    if w.q2k_idx is not None:
+        out.q2k_idx = np.ascontiguousarray(w.q2k_idx[:, :n])
+        out.q2k_num = np.ascontiguousarray(w.q2k_num[:, :n])
+    out.vbs = w.vbs
+    if w.block_map is not None:
+        out.block_map = w.block_map if w.block_map.ndim == 2 else np.ascontiguousarray(
+            w.block_map[:, :n])
+    return out
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     """bf16 tensor -> its uint16 bit patterns (a view, no rounding)."""
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
