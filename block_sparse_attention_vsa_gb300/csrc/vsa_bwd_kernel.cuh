@@ -38,14 +38,18 @@
 //   warps 8-11  dQ warps: thread = d column (TMEM lane of dQ^T).
 //   warp 12     TMA: K, V once; per step Q, dO (64 rows) and lse, D (64 floats) into a
 //               3-stage ring.
-//   warp 13     MMA issuer (one thread); owns the TMEM allocation.
-//   warp 14     list: compacts the block-map column into the step list (in chunks).
+//   warp 13     MMA issuer (one thread) of S^T, dP^T, dV, dK; owns the TMEM allocation.
+//   warp 14     list: compacts the block-map column into the step list (in chunks);
+//               during the steps its lane 0 issues the dQ^T MMAs (a second issuing
+//               thread: dQ^T depends on no other MMA of the step).
 // TMEM (512 columns): S^T 0-63 (P^T bf16 over 0-15 and 32-47), dP^T 64-127 (dS^T over
 // 64-79 and 96-111), dQ^T double buffer 128-255, dV 256-383, dK 384-511.
-// MMA issue order per step t: dV_t, S_{t+1}, dK_t, dQ_t, dP_{t+1}.  tcgen05 MMAs of one
-// thread execute in issue order, so S_{t+1} may overwrite the P^T that dV_t reads and
+// MMA issue order per step t on warp 13: dV_t, S_{t+1}, dK_t, dP_{t+1}.  tcgen05 MMAs of
+// one thread execute in issue order, so S_{t+1} may overwrite the P^T that dV_t reads and
 // dP_{t+1} the dS^T that dK_t reads; the commit behind S_{t+1} (dP_{t+1}) tells the
 // gradient warps both that S^T (dP^T) is ready and that its previous readers are done.
+// dQ_t, on warp 14, is ordered by barriers alone: it waits for dS^T of step t, and the
+// gradient warps overwrite the SMEM dS^T only after dQ_t has completed.
 // Every mbarrier wait is bounded; a wait that runs out records a code in the device
 // status word, raises the CTA's abort flag and every role returns.
 #pragma once
@@ -142,6 +146,7 @@ struct Ctl {
   uint64_t p_full, ds_full;  // the 8 gradient warps wrote P^T (dS^T)
   uint64_t dq_full[2], dq_empty[2];
   uint64_t acc_full, drain;
+  uint64_t drain_dq;  // every dQ^T MMA of the second issuing thread has completed
   uint64_t never;  // completed by nobody (the timeout test hook waits on it)
   int n_entries, go;
   uint32_t tmem_base;
@@ -236,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&ctl->acc_full, 1);
     mbar_init(&ctl->drain, 1);
+    mbar_init(&ctl->drain_dq, 1);
     mbar_init(&ctl->never, 1);
     ctl->abort_flag = 0;
     fence_mbar_init();
@@ -351,11 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);
         constexpr uint32_t kIdescG = idesc_bf16_f32(128, 128, false, true);
-        constexpr uint32_t kIdescQ = idesc_bf16_f32(128, 64, true, true);
         const uint64_t k_kmaj = smem_desc_sw128(smem_addr(smem + kOffK), 16, 1024);
         const uint64_t v_kmaj = smem_desc_sw128(smem_addr(smem + kOffV), 16, 1024);
-        const uint64_t k_mn = smem_desc_sw128(smem_addr(smem + kOffK), kKVTile / 2, 1024);
-        const uint64_t ds_mn = smem_desc_sw128(smem_addr(smem + kOffDS), 8192, 1024);
         if (g0 == 0 && !wait(&ctl->kv_full, 0, ctl, a, 0x42)) ok = false;
         if (ok && a.stall) {
           // test hook: wait on a barrier no role ever completes, so the wait runs out,
@@ -424,9 +427,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(tmem + kColDK, tmem + kColDP + 32 * (kk >> 1) + 8 * (kk & 1),
                    q_mn + ((kk * 2048) >> 4), kIdescG, (gg > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&ctl->ld_empty[st]);  // Q, dO, lse, D of the stage consumed
-          // dQ^T = K^T dS^T into dQ buffer gg & 1, K = keys in 8 steps
-          const uint32_t db = gg & 1;
-          if (gg >= 2 && !wait(&ctl->dq_empty[db], ((gg >> 1) + 1) & 1, ctl, a, 0x47)) {
+          if (i + 1 < n_steps) {  // dP^T of the next step (its copies have landed)
+            issue_sd(gg + 1, true);
+            mma_commit(&ctl->dp_full);
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    } else if (warp == kListWarp) {
+      // ---------------------------------------------------------------- dQ issue
+      // dQ^T = K^T dS^T (both operands MN-major in SMEM, K = keys in 8 steps) into dQ
+      // buffer gg & 1, on a second issuing thread: it depends on no other MMA of the step
+      // (dS^T comes from SMEM), and one thread alone cannot issue a step's 32 MMAs as fast
+      // as the tensor pipe runs them
+      if (lane == 0) {
+        constexpr uint32_t kIdescQ = idesc_bf16_f32(128, 64, true, true);
+        const uint64_t k_mn = smem_desc_sw128(smem_addr(smem + kOffK), kKVTile / 2, 1024);
+        const uint64_t ds_mn = smem_desc_sw128(smem_addr(smem + kOffDS), 8192, 1024);
+        if (g0 == 0 && !wait(&ctl->kv_full, 0, ctl, a, 0x51)) ok = false;
+        for (int i = 0; i < n_steps && ok; ++i) {
+          const uint32_t gg = g0 + i, db = gg & 1;
+          if (!wait(&ctl->ds_full, gg & 1, ctl, a, 0x52) ||
+              (gg >= 2 && !wait(&ctl->dq_empty[db], ((gg >> 1) + 1) & 1, ctl, a, 0x47))) {
             ok = false;
             break;
           }
@@ -436,10 +458,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(tmem + kColDQ + 64 * db, k_mn + ((k * 2048) >> 4), ds_mn + ((k * 2048) >> 4),
                    kIdescQ, k > 0 ? 1u : 0u);
           mma_commit(&ctl->dq_full[db]);
-          if (i + 1 < n_steps) {  // dP^T of the next step (its copies have landed)
-            issue_sd(gg + 1, true);
-            mma_commit(&ctl->dp_full);
-          }
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -508,6 +526,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
         tmem_st_32x32b_x16(tmem + lane_base + kColDP + 32 * wg, pk);
+        // the SMEM dS^T buffer is free once the previous step's dQ^T (issued by another
+        // thread, so not ordered behind this step's dP^T) has read it
+        if (gg >= 1 &&
+            !wait_warp(&ctl->dq_full[(gg - 1) & 1], ((gg - 1) >> 1) & 1, ctl, a, 0x50)) {
+          ok = false;
+          break;
+        }
         // dS^T row r, query columns 32 wg .. 32 wg + 31: 16-byte chunks 4 wg .. 4 wg + 3
         // of the 128-byte row, placed by the 128-byte swizzle (chunk ^ row % 8)
 #pragma unroll
@@ -557,6 +582,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every MMA issued has completed before TMEM can be released
       mma_commit(&ctl->drain);
       wait(&ctl->drain, 0, ctl, a, 0x4c, true);
+    }
+    __syncwarp();
+  } else if (warp == kListWarp) {
+    if (lane == 0) {  // every dQ^T MMA this thread issued has completed before TMEM goes
+      mma_commit(&ctl->drain_dq);
+      wait(&ctl->drain_dq, 0, ctl, a, 0x53, true);
     }
     __syncwarp();
   } else if (warp == kTmaWarp) {
