@@ -21,10 +21,10 @@
 //                     64 query rows a step.  Per step, on the 5th-generation tensor cores:
 //                       S^T  = K Q^T      (M = 128 keys, N = 64 queries, K = d) -> TMEM
 //                       dP^T = V dO^T                                           -> TMEM
-//                       P^T, dS^T formed by the gradient warps (one thread per key row)
-//                       and written back over S^T, dP^T as bf16; dS^T also to SMEM
+//                       P^T, dS^T formed by the gradient warps (one thread per key row);
+//                       P^T written back over S^T in TMEM as bf16, dS^T to SMEM
 //                       dV  += P^T dO     (A = P^T from TMEM, B = dO MN-major)
-//                       dK  += dS^T Q     (A = dS^T from TMEM, B = Q MN-major)
+//                       dK  += dS^T Q     (A = dS^T K-major in SMEM, B = Q MN-major)
 //                       dQ^T = K^T dS^T   (both operands MN-major in SMEM; M = 128 d)
 //                     and the dQ warps add dQ^T (one thread per d column, 64 query rows)
 //                     into an fp32 accumulator with coalesced reductions: several key tiles
@@ -38,18 +38,19 @@
 //   warps 8-11  dQ warps: thread = d column (TMEM lane of dQ^T).
 //   warp 12     TMA: K, V once; per step Q, dO (64 rows) and lse, D (64 floats) into a
 //               3-stage ring.
-//   warp 13     MMA issuer (one thread) of S^T, dP^T, dV, dK; owns the TMEM allocation.
+//   warp 13     MMA issuer (one thread) of S^T, dP^T, dV; owns the TMEM allocation.
 //   warp 14     list: compacts the block-map column into the step list (in chunks);
-//               during the steps its lane 0 issues the dQ^T MMAs (a second issuing
-//               thread: dQ^T depends on no other MMA of the step).
-// TMEM (512 columns): S^T 0-63 (P^T bf16 over 0-15 and 32-47), dP^T 64-127 (dS^T over
-// 64-79 and 96-111), dQ^T double buffer 128-255, dV 256-383, dK 384-511.
-// MMA issue order per step t on warp 13: dV_t, S_{t+1}, dK_t, dP_{t+1}.  tcgen05 MMAs of
-// one thread execute in issue order, so S_{t+1} may overwrite the P^T that dV_t reads and
-// dP_{t+1} the dS^T that dK_t reads; the commit behind S_{t+1} (dP_{t+1}) tells the
-// gradient warps both that S^T (dP^T) is ready and that its previous readers are done.
-// dQ_t, on warp 14, is ordered by barriers alone: it waits for dS^T of step t, and the
-// gradient warps overwrite the SMEM dS^T only after dQ_t has completed.
+//               during the steps its lane 0 issues the dK and dQ^T MMAs (a second
+//               issuing thread: they depend on no other MMA of the step).
+// TMEM (512 columns): S^T 0-63 (P^T bf16 over 0-15 and 32-47), dP^T 64-127, dQ^T double
+// buffer 128-255, dV 256-383, dK 384-511.  dS^T lives in SMEM only.
+// MMA issue order per step t on warp 13: dV_t, S_{t+1}, dP_{t+1}.  tcgen05 MMAs of one
+// thread execute in issue order, so S_{t+1} may overwrite the P^T that dV_t reads; dP_{t+1}
+// is issued once the gradient warps have read dP^T of step t (dS^T ready).  The commit
+// behind S_{t+1} (dP_{t+1}) tells the gradient warps that S^T (dP^T) is ready.  dK_t and
+// dQ_t, on warp 14, are ordered by barriers alone: they wait for dS^T of step t, and the
+// gradient warps overwrite the SMEM dS^T only after dQ_t (issued after dK_t) has
+// completed.  The Q/dO stage of a step is free once both threads' readers are done.
 // Every mbarrier wait is bounded; a wait that runs out records a code in the device
 // status word, raises the CTA's abort flag and every role returns.
 #pragma once
@@ -145,7 +146,7 @@ struct Ctl {
   uint64_t s_full, dp_full;  // S^T (dP^T) of the step is in TMEM; its previous readers are done
   uint64_t p_full, ds_full;  // the 8 gradient warps wrote P^T (dS^T)
   uint64_t dq_full[2], dq_empty[2];
-  uint64_t acc_full, drain;
+  uint64_t acc_full, acc_full_dk, drain;  // dV (dK) complete; every MMA of warp 13 done
   uint64_t drain_dq;  // every dQ^T MMA of the second issuing thread has completed
   uint64_t never;  // completed by nobody (the timeout test hook waits on it)
   int n_entries, go;
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->kv_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctl->ld_full[s], 1);
-      mbar_init(&ctl->ld_empty[s], 1);
+      mbar_init(&ctl->ld_empty[s], 2);  // one commit from each MMA-issuing thread
     }
     mbar_init(&ctl->s_full, 1);
     mbar_init(&ctl->dp_full, 1);
@@ -240,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->dq_empty[i], 4);
     }
     mbar_init(&ctl->acc_full, 1);
+    mbar_init(&ctl->acc_full_dk, 1);
     mbar_init(&ctl->drain, 1);
     mbar_init(&ctl->drain_dq, 1);
     mbar_init(&ctl->never, 1);
@@ -414,19 +416,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_sd(gn, false);
             mma_commit(&ctl->s_full);
           }
-          // dK += dS^T Q
+          mma_commit(&ctl->ld_empty[st]);  // this thread's readers of the stage are done
+          // dP^T of the next step overwrites this step's dP^T: the gradient warps have read
+          // it once dS^T is ready
           if (!wait(&ctl->ds_full, gg & 1, ctl, a, 0x46)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint64_t q_mn =
-              smem_desc_sw128(smem_addr(smem + kOffQ + st * kQTile), kQTile / 2, 1024);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + kColDK, tmem + kColDP + 32 * (kk >> 1) + 8 * (kk & 1),
-                   q_mn + ((kk * 2048) >> 4), kIdescG, (gg > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&ctl->ld_empty[st]);  // Q, dO, lse, D of the stage consumed
           if (i + 1 < n_steps) {  // dP^T of the next step (its copies have landed)
             issue_sd(gg + 1, true);
             mma_commit(&ctl->dp_full);
@@ -435,20 +431,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
     } else if (warp == kListWarp) {
-      // ---------------------------------------------------------------- dQ issue
-      // dQ^T = K^T dS^T (both operands MN-major in SMEM, K = keys in 8 steps) into dQ
-      // buffer gg & 1, on a second issuing thread: it depends on no other MMA of the step
-      // (dS^T comes from SMEM), and one thread alone cannot issue a step's 32 MMAs as fast
-      // as the tensor pipe runs them
+      // ---------------------------------------------------------------- dK, dQ issue
+      // The two contractions that take dS^T, on a second issuing thread: they depend on no
+      // other MMA of the step (dS^T comes from SMEM), and one thread alone cannot issue a
+      // step's 32 MMAs as fast as the tensor pipe runs them.
+      //   dK  += dS^T Q    (A = dS^T K-major, B = Q MN-major, K = queries in 4 steps)
+      //   dQ^T = K^T dS^T  (both MN-major, K = keys in 8 steps) into dQ buffer gg & 1
       if (lane == 0) {
+        constexpr uint32_t kIdescG = idesc_bf16_f32(128, 128, false, true);
         constexpr uint32_t kIdescQ = idesc_bf16_f32(128, 64, true, true);
         const uint64_t k_mn = smem_desc_sw128(smem_addr(smem + kOffK), kKVTile / 2, 1024);
         const uint64_t ds_mn = smem_desc_sw128(smem_addr(smem + kOffDS), 8192, 1024);
+        const uint64_t ds_kmaj = smem_desc_sw128(smem_addr(smem + kOffDS), 16, 1024);
         if (g0 == 0 && !wait(&ctl->kv_full, 0, ctl, a, 0x51)) ok = false;
         for (int i = 0; i < n_steps && ok; ++i) {
-          const uint32_t gg = g0 + i, db = gg & 1;
-          if (!wait(&ctl->ds_full, gg & 1, ctl, a, 0x52) ||
-              (gg >= 2 && !wait(&ctl->dq_empty[db], ((gg >> 1) + 1) & 1, ctl, a, 0x47))) {
+          const uint32_t gg = g0 + i, db = gg & 1, st = gg % kStages;
+          if (!wait(&ctl->ds_full, gg & 1, ctl, a, 0x52)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t q_mn =
+              smem_desc_sw128(smem_addr(smem + kOffQ + st * kQTile), kQTile / 2, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem + kColDK, ds_kmaj + ((kk * 32) >> 4), q_mn + ((kk * 2048) >> 4),
+                   kIdescG, (gg > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&ctl->ld_empty[st]);  // this thread's readers of the stage are done
+          if (gg >= 2 && !wait(&ctl->dq_empty[db], ((gg >> 1) + 1) & 1, ctl, a, 0x47)) {
             ok = false;
             break;
           }
@@ -525,7 +535,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
-        tmem_st_32x32b_x16(tmem + lane_base + kColDP + 32 * wg, pk);
         // the SMEM dS^T buffer is free once the previous step's dQ^T (issued by another
         // thread, so not ordered behind this step's dP^T) has read it
         if (gg >= 1 &&
@@ -541,7 +550,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(ds_row + phys * 16) =
               make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         }
-        tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
@@ -585,7 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == kListWarp) {
-    if (lane == 0) {  // every dQ^T MMA this thread issued has completed before TMEM goes
+    if (lane == 0) {  // every MMA this thread issued has completed before TMEM goes
+      if (any && ok) mma_commit(&ctl->acc_full_dk);
       mma_commit(&ctl->drain_dq);
       wait(&ctl->drain_dq, 0, ctl, a, 0x53, true);
     }
@@ -604,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint16_t* dst = (is_dk ? a.dk : a.dv) + ((long long)bkv * a.Sk + 128 * tile + r) * 128;
     bool have = false;
     if (any && ok) {
-      have = wait_warp(&ctl->acc_full, 0, ctl, a, 0x4f);
+      have = wait_warp(is_dk ? &ctl->acc_full_dk : &ctl->acc_full, 0, ctl, a, 0x4f);
       tc_fence_after();
     }
     if (have || !any) {
