@@ -464,7 +464,7 @@ def main():
                 "peak_source": f"{peak_src} dense bf16 (burst)",
                 "kernel": "bsa_bwd_kernel (whole vsa_bwd call timed)" if bwd else "bsa_fwd_kernel"}
     if bwd:
-        roofline["traffic"] = None
+        roofline["traffic"] = TRAFFIC_BWD.get(w.name)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and bwd:
@@ -507,7 +507,10 @@ def main():
 
 # DRAM bytes (read + write) per launch of the forward kernel, from an ncu capture of the
 # same kernel build on the same workload; absent = not measured for the current kernel.
-TRAFFIC = {"vsa_mid": 182.9e6, "vsa_blk128": 1611.2e6}
+TRAFFIC = {"vsa_long_video": 2462.8e6,  # captured on 4 of 24 heads, scaled by 6
+           "jenga": 385.2e6, "vsa_mid": 183.6e6, "vsa_blk128": 1609.1e6}
+# the same for the backward kernel (bsa_bwd_kernel), per launch
+TRAFFIC_BWD = {"vsa_mid": 456.4e6}
 
 
 if __name__ == "__main__":
