@@ -42,15 +42,18 @@
 //   warp 14     list: compacts the block-map column into the step list (in chunks);
 //               during the steps its lane 0 issues the dK and dQ^T MMAs (a second
 //               issuing thread: they depend on no other MMA of the step).
-// TMEM (512 columns): S^T 0-63 (P^T bf16 over 0-15 and 32-47), dP^T 64-127, dQ^T double
-// buffer 128-255, dV 256-383, dK 384-511.  dS^T lives in SMEM only.
-// MMA issue order per step t on warp 13: dV_t, S_{t+1}, dP_{t+1}.  tcgen05 MMAs of one
-// thread execute in issue order, so S_{t+1} may overwrite the P^T that dV_t reads; dP_{t+1}
-// is issued once the gradient warps have read dP^T of step t (dS^T ready).  The commit
-// behind S_{t+1} (dP_{t+1}) tells the gradient warps that S^T (dP^T) is ready.  dK_t and
-// dQ_t, on warp 14, are ordered by barriers alone: they wait for dS^T of step t, and the
-// gradient warps overwrite the SMEM dS^T only after dQ_t (issued after dK_t) has
-// completed.  The Q/dO stage of a step is free once both threads' readers are done.
+// TMEM (512 columns): two step slots (step g uses slot g & 1) at 0 and 128, each holding
+// S^T in its first 64 columns (P^T bf16 over 0-15 and 32-47) and dP^T in the next 64 (then
+// dQ^T of the same step, written over the consumed dP^T); dV 256-383, dK 384-511.  dS^T
+// lives in SMEM only, one tile per slot.
+// MMA issue order on warp 13: S_0, dP_0, then per step t: S_{t+1}, dV_t, dP_{t+1}, so the
+// next step's S^T is computed while the gradient warps form P^T and dS^T of this one.
+// tcgen05 MMAs of one thread execute in issue order: S_{t+2} lands in the slot whose P^T dV_t
+// read.  dP_{t+1} waits until the dQ warps have read dQ^T of step t - 1 out of its columns.
+// dK_t and dQ_t, on warp 14, are ordered by barriers alone: they wait for dS^T of step t
+// (which comes after the gradient warps read dP^T_t), and the gradient warps overwrite a
+// slot's SMEM dS^T only after dQ_{t-2} (issued after dK_{t-2}) has completed.  The Q/dO
+// stage of a step is free once both threads' readers are done.
 // Every mbarrier wait is bounded; a wait that runs out records a code in the device
 // status word, raises the CTA's abort flag and every role returns.
 #pragma once
@@ -131,21 +134,25 @@ constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kKVTile;
 constexpr uint32_t kOffQ = 2 * kKVTile;                  // [kStages]
 constexpr uint32_t kOffDO = kOffQ + kStages * kQTile;    // [kStages]
-constexpr uint32_t kOffDS = kOffDO + kStages * kQTile;   // dS^T [128 keys][64 queries] bf16
-constexpr uint32_t kOffRow = kOffDS + 128 * 64 * 2;      // [kStages] lse[64], D[64]
+constexpr uint32_t kDSTile = 128 * 64 * 2;               // dS^T [128 keys][64 queries] bf16
+constexpr uint32_t kOffDS = kOffDO + kStages * kQTile;   // dS^T [2] (one per step slot)
+constexpr uint32_t kOffRow = kOffDS + 2 * kDSTile;       // [kStages] lse[64], D[64]
 constexpr uint32_t kOffList = kOffRow + kStages * 512;
 constexpr uint32_t kOffCtl = kOffList + kMaxEntries * 4;
 constexpr uint32_t kSmemBytes = kOffCtl + 1024 + 1024;  // + alignment slack
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kColDV = 256, kColDK = 384;
+// two step slots: slot b (steps g with g & 1 == b) holds S^T (then the step's P^T) at
+// 128 b and dP^T (then the step's dQ^T) at 128 b + 64
+constexpr uint32_t kColSlot = 128, kColDPOff = 64, kColDV = 256, kColDK = 384;
 
 struct Ctl {
   uint64_t kv_full;
   uint64_t ld_full[kStages], ld_empty[kStages];
-  uint64_t s_full, dp_full;  // S^T (dP^T) of the step is in TMEM; its previous readers are done
-  uint64_t p_full, ds_full;  // the 8 gradient warps wrote P^T (dS^T)
-  uint64_t dq_full[2], dq_empty[2];
+  // per step slot b (one phase per step of that slot)
+  uint64_t s_full[2], dp_full[2];    // S^T (dP^T) of the step is in TMEM
+  uint64_t p_full[2], ds_full[2];    // the 8 gradient warps wrote P^T (TMEM) / dS^T (SMEM)
+  uint64_t dq_full[2], dq_empty[2];  // dK, dQ^T of the step done (dS^T read) / dQ^T read out
   uint64_t acc_full, acc_full_dk, drain;  // dV (dK) complete; every MMA of warp 13 done
   uint64_t drain_dq;  // every dQ^T MMA of the second issuing thread has completed
   uint64_t never;  // completed by nobody (the timeout test hook waits on it)
@@ -232,11 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->ld_full[s], 1);
       mbar_init(&ctl->ld_empty[s], 2);  // one commit from each MMA-issuing thread
     }
-    mbar_init(&ctl->s_full, 1);
-    mbar_init(&ctl->dp_full, 1);
-    mbar_init(&ctl->p_full, 8);
-    mbar_init(&ctl->ds_full, 8);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->s_full[i], 1);
+      mbar_init(&ctl->dp_full[i], 1);
+      mbar_init(&ctl->p_full[i], 8);
+      mbar_init(&ctl->ds_full[i], 8);
       mbar_init(&ctl->dq_full[i], 1);
       mbar_init(&ctl->dq_empty[i], 4);
     }
@@ -368,9 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           wait(&ctl->never, 0, ctl, a, 0x5f);
           ok = false;
         }
-        // S^T (dP^T) of step gg: A = K (V) K-major, B = Q (dO) K-major, K = d in 8 steps
+        // S^T (dP^T) of step gg into its slot: A = K (V) K-major, B = Q (dO) K-major,
+        // K = d in 8 steps
         auto issue_sd = [&](uint32_t gg, bool dp) {
-          const uint32_t st = gg % kStages;
+          const uint32_t st = gg % kStages, b = gg & 1;
           const uint64_t ad = dp ? v_kmaj : k_kmaj;
           const uint64_t bd =
               smem_desc_sw128(smem_addr(smem + (dp ? kOffDO : kOffQ) + st * kQTile), 16, 1024);
@@ -378,54 +386,62 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 8; ++k) {
             const uint64_t oa = ((k >> 2) * (kKVTile / 2) + (k & 3) * 32) >> 4;
             const uint64_t ob = ((k >> 2) * (kQTile / 2) + (k & 3) * 32) >> 4;
-            mma_ss(tmem + (dp ? kColDP : kColS), ad + oa, bd + ob, kIdescS, k > 0 ? 1u : 0u);
+            mma_ss(tmem + kColSlot * b + (dp ? kColDPOff : 0u), ad + oa, bd + ob, kIdescS,
+                   k > 0 ? 1u : 0u);
           }
+          mma_commit(dp ? &ctl->dp_full[b] : &ctl->s_full[b]);
+        };
+        // the step's Q, dO have landed
+        auto landed = [&](uint32_t gg) {
+          return wait(&ctl->ld_full[gg % kStages], (gg / kStages) & 1, ctl, a, 0x43);
+        };
+        // dP^T of step gg overwrites the slot's dQ^T of step gg - 2: read out by then
+        auto dq_read = [&](uint32_t gg) {
+          return gg < 2 || wait(&ctl->dq_empty[gg & 1], ((gg - 2) >> 1) & 1, ctl, a, 0x47);
         };
         if (ok) {
-          if (!wait(&ctl->ld_full[g0 % kStages], (g0 / kStages) & 1, ctl, a, 0x43)) {
+          if (!landed(g0) || !dq_read(g0)) {
             ok = false;
           } else {
             tc_fence_after();
             issue_sd(g0, false);
-            mma_commit(&ctl->s_full);
             issue_sd(g0, true);
-            mma_commit(&ctl->dp_full);
           }
         }
         for (int i = 0; i < n_steps && ok; ++i) {
-          const uint32_t gg = g0 + i, st = gg % kStages;
+          const uint32_t gg = g0 + i, st = gg % kStages, b = gg & 1;
+          // S^T of the next step into the other slot, ahead of this step's dV: that slot's
+          // previous P^T (step gg - 1) was read by dV issued earlier on this thread
+          if (i + 1 < n_steps) {
+            if (!landed(gg + 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_sd(gg + 1, false);
+          }
           // dV += P^T dO: A = P^T (TMEM, 64 query columns as 32 packed), B = dO MN-major
-          if (!wait(&ctl->p_full, gg & 1, ctl, a, 0x44)) {
+          if (!wait(&ctl->p_full[b], (gg >> 1) & 1, ctl, a, 0x44)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint64_t do_mn =
               smem_desc_sw128(smem_addr(smem + kOffDO + st * kQTile), kQTile / 2, 1024);
+          const uint32_t tS = tmem + kColSlot * b;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + kColDV, tmem + kColS + 32 * (kk >> 1) + 8 * (kk & 1),
+            mma_ts(tmem + kColDV, tS + 32 * (kk >> 1) + 8 * (kk & 1),
                    do_mn + ((kk * 2048) >> 4), kIdescG, (gg > 0 || kk > 0) ? 1u : 0u);
-          if (i + 1 < n_steps) {  // S^T of the next step
-            const uint32_t gn = gg + 1;
-            if (!wait(&ctl->ld_full[gn % kStages], (gn / kStages) & 1, ctl, a, 0x45)) {
+          mma_commit(&ctl->ld_empty[st]);  // this thread's readers of the stage are done
+          // dP^T of the next step into the other slot once its dQ^T (step gg - 1) is out
+          if (i + 1 < n_steps) {
+            if (!dq_read(gg + 1)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            issue_sd(gn, false);
-            mma_commit(&ctl->s_full);
-          }
-          mma_commit(&ctl->ld_empty[st]);  // this thread's readers of the stage are done
-          // dP^T of the next step overwrites this step's dP^T: the gradient warps have read
-          // it once dS^T is ready
-          if (!wait(&ctl->ds_full, gg & 1, ctl, a, 0x46)) {
-            ok = false;
-            break;
-          }
-          if (i + 1 < n_steps) {  // dP^T of the next step (its copies have landed)
             issue_sd(gg + 1, true);
-            mma_commit(&ctl->dp_full);
           }
         }
       }
@@ -436,17 +452,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // other MMA of the step (dS^T comes from SMEM), and one thread alone cannot issue a
       // step's 32 MMAs as fast as the tensor pipe runs them.
       //   dK  += dS^T Q    (A = dS^T K-major, B = Q MN-major, K = queries in 4 steps)
-      //   dQ^T = K^T dS^T  (both MN-major, K = keys in 8 steps) into dQ buffer gg & 1
+      //   dQ^T = K^T dS^T  (both MN-major, K = keys in 8 steps) over the step slot's dP^T
       if (lane == 0) {
         constexpr uint32_t kIdescG = idesc_bf16_f32(128, 128, false, true);
         constexpr uint32_t kIdescQ = idesc_bf16_f32(128, 64, true, true);
         const uint64_t k_mn = smem_desc_sw128(smem_addr(smem + kOffK), kKVTile / 2, 1024);
-        const uint64_t ds_mn = smem_desc_sw128(smem_addr(smem + kOffDS), 8192, 1024);
-        const uint64_t ds_kmaj = smem_desc_sw128(smem_addr(smem + kOffDS), 16, 1024);
         if (g0 == 0 && !wait(&ctl->kv_full, 0, ctl, a, 0x51)) ok = false;
         for (int i = 0; i < n_steps && ok; ++i) {
           const uint32_t gg = g0 + i, db = gg & 1, st = gg % kStages;
-          if (!wait(&ctl->ds_full, gg & 1, ctl, a, 0x52)) {
+          const uint64_t ds_mn = smem_desc_sw128(smem_addr(smem + kOffDS + db * kDSTile), 8192, 1024);
+          const uint64_t ds_kmaj = smem_desc_sw128(smem_addr(smem + kOffDS + db * kDSTile), 16, 1024);
+          if (!wait(&ctl->ds_full[db], (gg >> 1) & 1, ctl, a, 0x52)) {
             ok = false;
             break;
           }
@@ -458,15 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(tmem + kColDK, ds_kmaj + ((kk * 32) >> 4), q_mn + ((kk * 2048) >> 4),
                    kIdescG, (gg > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&ctl->ld_empty[st]);  // this thread's readers of the stage are done
-          if (gg >= 2 && !wait(&ctl->dq_empty[db], ((gg >> 1) + 1) & 1, ctl, a, 0x47)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+          // dQ^T over the slot's dP^T, which the gradient warps have read (dS^T is ready)
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + kColDQ + 64 * db, k_mn + ((k * 2048) >> 4), ds_mn + ((k * 2048) >> 4),
-                   kIdescQ, k > 0 ? 1u : 0u);
+            mma_ss(tmem + kColSlot * db + kColDPOff, k_mn + ((k * 2048) >> 4),
+                   ds_mn + ((k * 2048) >> 4), kIdescQ, k > 0 ? 1u : 0u);
           mma_commit(&ctl->dq_full[db]);
         }
       }
@@ -477,9 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = (warp & 3) * 32 + (int)lane;  // key row of the tile
       const int kbi = BLOCK == 64 ? (r >> 6) : 0;
       const bool key_ok = (r & (BLOCK - 1)) < vk[kbi];
-      uint8_t* ds_row = smem + kOffDS + (r >> 3) * 1024 + (r & 7) * 128;
       for (int i = 0; i < n_steps; ++i) {
-        const uint32_t gg = g0 + i, st = gg % kStages;
+        const uint32_t gg = g0 + i, st = gg % kStages, b = gg & 1;
+        const uint32_t tS = tmem + lane_base + kColSlot * b + 32 * wg, tDP = tS + kColDPOff;
+        uint8_t* ds_row = smem + kOffDS + b * kDSTile + (r >> 3) * 1024 + (r & 7) * 128;
         const uint32_t e = list[i / kSubQ];
         const bool valid = key_ok && ((e >> (16 + kbi)) & 1u);
         const float* lse_s = reinterpret_cast<const float*>(smem + kOffRow + st * 512) + 32 * wg;
@@ -487,13 +500,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // lse and D of the step have landed (the stage is not refilled before dK of this
         // step, which waits for this warp), and S^T is in TMEM
         if (!wait_warp(&ctl->ld_full[st], (gg / kStages) & 1, ctl, a, 0x48) ||
-            !wait_warp(&ctl->s_full, gg & 1, ctl, a, 0x49)) {
+            !wait_warp(&ctl->s_full[b], (gg >> 1) & 1, ctl, a, 0x49)) {
           ok = false;
           break;
         }
         tc_fence_after();
         uint32_t sr[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + kColS + 32 * wg, sr);
+        tmem_ld_32x32b_x32(tS, sr);
         tmem_wait_ld();
         float p[32];
 #pragma unroll
@@ -511,17 +524,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
-        tmem_st_32x32b_x16(tmem + lane_base + kColS + 32 * wg, pk);
+        tmem_st_32x32b_x16(tS, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->p_full);
-        if (!wait_warp(&ctl->dp_full, gg & 1, ctl, a, 0x4a)) {
+        if (lane == 0) mbar_arrive(&ctl->p_full[b]);
+        if (!wait_warp(&ctl->dp_full[b], (gg >> 1) & 1, ctl, a, 0x4a)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        tmem_ld_32x32b_x32(tmem + lane_base + kColDP + 32 * wg, sr);
+        tmem_ld_32x32b_x32(tDP, sr);
         tmem_wait_ld();
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
@@ -535,10 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
-        // the SMEM dS^T buffer is free once the previous step's dQ^T (issued by another
-        // thread, so not ordered behind this step's dP^T) has read it
-        if (gg >= 1 &&
-            !wait_warp(&ctl->dq_full[(gg - 1) & 1], ((gg - 1) >> 1) & 1, ctl, a, 0x50)) {
+        // the slot's SMEM dS^T tile is free once dK and dQ^T of step gg - 2 have read it
+        if (gg >= 2 && !wait_warp(&ctl->dq_full[b], ((gg - 2) >> 1) & 1, ctl, a, 0x50)) {
           ok = false;
           break;
         }
@@ -553,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->ds_full);
+        if (lane == 0) mbar_arrive(&ctl->ds_full[b]);
       }
     } else if (warp >= kDqWarp0 && warp < kDqWarp0 + 4) {
       // ---------------------------------------------------------------- dQ reductions
@@ -567,8 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         uint32_t v0[32], v1[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + kColDQ + 64 * db, v0);
-        tmem_ld_32x32b_x32(tmem + lane_base + kColDQ + 64 * db + 32, v1);
+        tmem_ld_32x32b_x32(tmem + lane_base + kColSlot * db + kColDPOff, v0);
+        tmem_ld_32x32b_x32(tmem + lane_base + kColSlot * db + kColDPOff + 32, v1);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
