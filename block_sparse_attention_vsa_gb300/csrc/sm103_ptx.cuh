@@ -309,6 +309,11 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 // bf16x2 word -> the two values as an fp32 pair (exact widening)
 __device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
   return f32x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));

@@ -375,7 +375,7 @@ BwdLayout bwd_layout(long long B, long long Hq, long long Sq, long long Sk, int 
   BwdLayout l;
   l.bitmap = 0;
   l.dvec = align256((size_t)(B * Hq * nbq * nbk));
-  l.dq = l.dvec + align256((size_t)rows * 4);
+  l.dq = l.dvec + align256((size_t)rows * 8);  // -D, then -lse
   l.total = l.dq + (size_t)rows * 128 * 4;
   return l;
 }
@@ -503,17 +503,18 @@ vsa_status vsa_bwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int8_t* bitmap = reinterpret_cast<int8_t*>(ws + lay.bitmap);
-  float* Dv = reinterpret_cast<float*>(ws + lay.dvec);
   float* dq_acc = reinterpret_cast<float*>(ws + lay.dq);
   const int nbq = Sq / block, nbk = Sk / block;
   const long long lut_rows = (long long)B * Hq * nbq, rows = p.rows_q();
+  float* nD = reinterpret_cast<float*>(ws + lay.dvec);
+  float* nlse = nD + rows;
   int launches = 0;
   if (nbk > 0) {
     lut_to_bitmap_kernel<<<(unsigned)lut_rows, 128, 0, s>>>(q2k_idx, q2k_num, max_kv, nbk,
                                                             bitmap);
     ++launches;
   }
-  bwd_prep_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(out, dout, rows, Dv);
+  bwd_prep_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(out, dout, lse, rows, nD, nlse);
   ++launches;
   if (cudaGetLastError() != cudaSuccess ||
       cudaMemsetAsync(dq_acc, 0, (size_t)rows * 128 * 4, s) != cudaSuccess)
@@ -521,8 +522,8 @@ vsa_status vsa_bwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
   unsigned int* status = status_word();
   if (status == nullptr) return VSA_ERR_CUDA;
   BwdArgs a{};
-  a.lse = lse;
-  a.Dv = Dv;
+  a.nlse = nlse;
+  a.nD = nD;
   a.bitmap = bitmap;
   a.vbs = variable_block_sizes;
   a.dq_acc = dq_acc;
@@ -547,7 +548,7 @@ vsa_status vsa_bwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
   if (st != VSA_OK) return st;
   if (n_ctas > 0) ++launches;
   const long long n8 = rows * 16;
-  bwd_dq_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, s>>>(dq_acc, n8, dq);
+  bwd_dq_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, s>>>(dq_acc, n8, scale, dq);
   if (cudaGetLastError() != cudaSuccess) return VSA_ERR_CUDA;
   t_last_launches = launches + 1;
   return VSA_OK;

@@ -10,7 +10,8 @@
 // with dk and dv summed over every query head of a key/value group.
 //
 // Kernels:
-//   bwd_prep_kernel   D_i for every query row (one warp per row).
+//   bwd_prep_kernel   per query row, one warp each: -D_i, and -lse_i (-inf for a row that
+//                     attends no key, so that every p of the row comes out 0).
 //   bsa_bwd_kernel    one CTA per (batch, key/value head, key tile of 128 keys): a tile is
 //                     one key block (block 128) or an adjacent pair of key blocks (block
 //                     64: the pair walks the union of the query blocks either selects, and
@@ -22,14 +23,15 @@
 //                       S^T  = K Q^T      (M = 128 keys, N = 64 queries, K = d) -> TMEM
 //                       dP^T = V dO^T                                           -> TMEM
 //                       P^T, dS^T formed by the gradient warps (one thread per key row);
-//                       P^T written back over S^T in TMEM as bf16, dS^T to SMEM
+//                       P^T written back over S^T in TMEM as bf16, dS^T to SMEM (without
+//                       the factor scale, which the dK epilogue and bwd_dq_kernel apply)
 //                       dV  += P^T dO     (A = P^T from TMEM, B = dO MN-major)
 //                       dK  += dS^T Q     (A = dS^T K-major in SMEM, B = Q MN-major)
 //                       dQ^T = K^T dS^T   (both operands MN-major in SMEM; M = 128 d)
 //                     and the dQ warps add dQ^T (one thread per d column, 64 query rows)
 //                     into an fp32 accumulator with coalesced reductions: several key tiles
 //                     feed every query row.
-//   bwd_dq_kernel     fp32 dQ accumulator -> bf16 dq.
+//   bwd_dq_kernel     fp32 dQ accumulator times scale -> bf16 dq.
 //
 // bsa_bwd_kernel roles (15 warps):
 //   warps 0-7   gradient warps: warpgroup w handles query columns 32w..32w+31 of a step,
@@ -66,10 +68,13 @@
 
 namespace vsa {
 
-// D_i = sum_d dout[i][d] * out[i][d] for rows rows; one warp per row, 4 elements per lane.
+// For rows rows, one warp per row (4 elements per lane): nD[i] = -sum_d dout[i][d] out[i][d]
+// and nlse[i] = -lse[i], or -inf where lse[i] is -inf (a row that attends no key).
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restrict__ out,
                                                        const uint16_t* __restrict__ dout,
-                                                       long long rows, float* __restrict__ Dv) {
+                                                       const float* __restrict__ lse,
+                                                       long long rows, float* __restrict__ nD,
+                                                       float* __restrict__ nlse) {
   const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (r >= rows) return;
   const uint32_t lane = threadIdx.x & 31;
@@ -84,27 +89,32 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
   }
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) Dv[r] = acc;
+  if (lane == 0) {
+    nD[r] = -acc;
+    const float l = lse[r];
+    nlse[r] = l > -3.0e38f ? -l : -INFINITY;
+  }
 }
 
-// fp32 dQ accumulator -> bf16 (round to nearest even), 8 elements per thread.
+// scale times the fp32 dQ accumulator -> bf16 (round to nearest even), 8 elements per thread.
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ acc,
-                                                     long long n8, uint16_t* __restrict__ dq) {
+                                                     long long n8, float scale,
+                                                     uint16_t* __restrict__ dq) {
   const long long i = (long long)blockIdx.x * 256 + threadIdx.x;
   if (i >= n8) return;
   const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
   const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
   uint4 o;
-  o.x = pack_bf16x2(a.x, a.y);
-  o.y = pack_bf16x2(a.z, a.w);
-  o.z = pack_bf16x2(b.x, b.y);
-  o.w = pack_bf16x2(b.z, b.w);
+  o.x = pack_bf16x2(a.x * scale, a.y * scale);
+  o.y = pack_bf16x2(a.z * scale, a.w * scale);
+  o.z = pack_bf16x2(b.x * scale, b.y * scale);
+  o.w = pack_bf16x2(b.z * scale, b.w * scale);
   reinterpret_cast<uint4*>(dq)[i] = o;
 }
 
 struct BwdArgs {
-  const float* lse;         // [B*Hq*Sq], base 2, from the forward
-  const float* Dv;          // [B*Hq*Sq]
+  const float* nlse;        // [B*Hq*Sq] -lse (base 2), -inf for a row that attends no key
+  const float* nD;          // [B*Hq*Sq] -D
   const int8_t* bitmap;     // [B*Hq*nbq, nbk] 0/1 block map
   const int32_t* vbs;       // [nbk] or null
   float* dq_acc;            // [B*Hq*Sq, 128] fp32, zeroed
@@ -136,7 +146,7 @@ constexpr uint32_t kOffQ = 2 * kKVTile;                  // [kStages]
 constexpr uint32_t kOffDO = kOffQ + kStages * kQTile;    // [kStages]
 constexpr uint32_t kDSTile = 128 * 64 * 2;               // dS^T [128 keys][64 queries] bf16
 constexpr uint32_t kOffDS = kOffDO + kStages * kQTile;   // dS^T [2] (one per step slot)
-constexpr uint32_t kOffRow = kOffDS + 2 * kDSTile;       // [kStages] lse[64], D[64]
+constexpr uint32_t kOffRow = kOffDS + 2 * kDSTile;       // [kStages] -lse[64], -D[64]
 constexpr uint32_t kOffList = kOffRow + kStages * 512;
 constexpr uint32_t kOffCtl = kOffList + kMaxEntries * 4;
 constexpr uint32_t kSmemBytes = kOffCtl + 1024 + 1024;  // + alignment slack
@@ -355,8 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(qs + kQTile / 2, &tq, &ctl->ld_full[st], 64, (int)row0);
           tma_load_2d(os, &tdo, &ctl->ld_full[st], 0, (int)row0);
           tma_load_2d(os + kQTile / 2, &tdo, &ctl->ld_full[st], 64, (int)row0);
-          bulk_load(rs, a.lse + row0, 256, &ctl->ld_full[st]);
-          bulk_load(rs + 64, a.Dv + row0, 256, &ctl->ld_full[st]);
+          bulk_load(rs, a.nlse + row0, 256, &ctl->ld_full[st]);
+          bulk_load(rs + 64, a.nD + row0, 256, &ctl->ld_full[st]);
           ++fills[st];
         }
       }
@@ -495,9 +505,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* ds_row = smem + kOffDS + b * kDSTile + (r >> 3) * 1024 + (r & 7) * 128;
         const uint32_t e = list[i / kSubQ];
         const bool valid = key_ok && ((e >> (16 + kbi)) & 1u);
-        const float* lse_s = reinterpret_cast<const float*>(smem + kOffRow + st * 512) + 32 * wg;
-        const float* D_s = lse_s + 64;
-        // lse and D of the step have landed (the stage is not refilled before dK of this
+        const float* nlse_s = reinterpret_cast<const float*>(smem + kOffRow + st * 512) + 32 * wg;
+        const float* nD_s = nlse_s + 64;
+        // -lse and -D of the step have landed (the stage is not refilled before dK of this
         // step, which waits for this warp), and S^T is in TMEM
         if (!wait_warp(&ctl->ld_full[st], (gg / kStages) & 1, ctl, a, 0x48) ||
             !wait_warp(&ctl->s_full[b], (gg >> 1) & 1, ctl, a, 0x49)) {
@@ -508,18 +518,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sr[32];
         tmem_ld_32x32b_x32(tS, sr);
         tmem_wait_ld();
+        // p = 2^(s scale log2(e) - lse): pairs of columns per fp32x2 instruction; a key the
+        // query block did not select gives 0, and so does a row with no attended key
+        // (its -lse is -inf)
         float p[32];
+        if (valid) {
+          const uint64_t c2 = f32x2(a.scale_log2, a.scale_log2);
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 l4 = reinterpret_cast<const float4*>(lse_s)[c4];
-          const float l[4] = {l4.x, l4.y, l4.z, l4.w};
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 l4 = reinterpret_cast<const float4*>(nlse_s)[c4];
+            const int c = 4 * c4;
+            const uint64_t x01 = fma_f32x2(
+                f32x2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, f32x2(l4.x, l4.y));
+            const uint64_t x23 = fma_f32x2(
+                f32x2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), c2, f32x2(l4.z, l4.w));
+            float x[4];
+            split_f32x2(x01, x[0], x[1]);
+            split_f32x2(x23, x[2], x[3]);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int c = 4 * c4 + j;
-            p[c] = (valid && l[j] > -3.0e38f)
-                       ? fast_exp2(fmaf(__uint_as_float(sr[c]), a.scale_log2, -l[j]))
-                       : 0.0f;
+            for (int j = 0; j < 4; ++j) p[c + j] = fast_exp2(x[j]);
           }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) p[c] = 0.0f;
         }
         uint32_t pk[16];
 #pragma unroll
@@ -536,14 +557,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_ld_32x32b_x32(tDP, sr);
         tmem_wait_ld();
+        if (valid) {  // dS = p (dP - D), without the factor scale
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 d4 = reinterpret_cast<const float4*>(D_s)[c4];
-          const float d[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int c = 4 * c4 + j;
-            p[c] = p[c] * (__uint_as_float(sr[c]) - d[j]) * a.scale;  // dS, scaled
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 d4 = reinterpret_cast<const float4*>(nD_s)[c4];
+            const int c = 4 * c4;
+            const uint64_t t01 = add_f32x2(
+                f32x2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), f32x2(d4.x, d4.y));
+            const uint64_t t23 = add_f32x2(
+                f32x2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), f32x2(d4.z, d4.w));
+            split_f32x2(mul_f32x2(f32x2(p[c], p[c + 1]), t01), p[c], p[c + 1]);
+            split_f32x2(mul_f32x2(f32x2(p[c + 2], p[c + 3]), t23), p[c + 2], p[c + 3]);
           }
         }
 #pragma unroll
@@ -594,6 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ------------------------------------------------------------------ dK, dV epilogue
+  // (dK takes the factor scale that dS^T left out)
   const bool any = g > 0;
   if (warp == kMmaWarp) {
     if (lane == 0) {
@@ -621,6 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = (warp & 3) * 32 + (int)lane;
     const bool is_dk = warp >= 4;
     const bool row_ok = 128 * tile + r < a.Sk;  // a lone last block-64 key block
+    const float sc = is_dk ? a.scale : 1.0f;
     uint16_t* dst = (is_dk ? a.dk : a.dv) + ((long long)bkv * a.Sk + 128 * tile + r) * 128;
     bool have = false;
     if (any && ok) {
@@ -642,10 +668,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             reinterpret_cast<uint4*>(dst + 32 * c)[j] = make_uint4(
-                pack_bf16x2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
-                pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
-                pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
-                pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+                pack_bf16x2(__uint_as_float(v[8 * j]) * sc, __uint_as_float(v[8 * j + 1]) * sc),
+                pack_bf16x2(__uint_as_float(v[8 * j + 2]) * sc, __uint_as_float(v[8 * j + 3]) * sc),
+                pack_bf16x2(__uint_as_float(v[8 * j + 4]) * sc, __uint_as_float(v[8 * j + 5]) * sc),
+                pack_bf16x2(__uint_as_float(v[8 * j + 6]) * sc, __uint_as_float(v[8 * j + 7]) * sc));
         }
       }
     }

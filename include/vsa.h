@@ -205,8 +205,8 @@ VSA_API size_t vsa_split_workspace_bytes(int B, int Hq, int Sq, int block, int n
  *   dout         [B, Hq, Sq, D] bf16.
  *   dq           [B, Hq, Sq, D] bf16 output;  dk, dv  [B, Hkv, Sk, D] bf16 outputs.
  *   workspace    at least vsa_bwd_workspace_bytes(B, Hq, Sq, Sk, block) bytes, 256-byte
- *                aligned, no initialisation needed (the block map, D and an fp32 dq
- *                accumulator live there).
+ *                aligned, no initialisation needed (the block map, -D and -lse per
+ *                query row and an fp32 dq accumulator live there).
  *   No output may overlap an input or another output.  Enqueues up to four kernels and
  *   one memset; errors as vsa_fwd_gqa, and VSA_ERR_UNSUPPORTED for more than 65536 query
  *   blocks per head or more than 4096 query heads per key/value head.

@@ -166,9 +166,10 @@ def test_bwd_validation(lib):
     assert _bwd(lib, Hkv=3) == binding.VSA_ERR_INVALID_ARG
     assert _bwd(lib, Sk=100) == binding.VSA_ERR_INVALID_ARG
     assert _bwd(lib, B=0) == binding.VSA_OK
-    # block map B*Hq*nbq*nbk bytes, D per row, fp32 dq accumulator (each 256-aligned)
+    # block map B*Hq*nbq*nbk bytes, -D and -lse per row, fp32 dq accumulator (each
+    # 256-aligned)
     n = lib.vsa_bwd_workspace_bytes(1, 2, 256, 512, 64)
-    assert n == 256 + 2 * 256 * 4 + 2 * 256 * 128 * 4
+    assert n == 256 + 2 * 256 * 8 + 2 * 256 * 128 * 4
     assert lib.vsa_bwd_workspace_bytes(1, 2, 256, 500, 64) == 0
     # the step list holds a query block in 16 bits and a head of the group in 12
     assert _bwd(lib, Sq=64 * 65537, Hq=1) == binding.VSA_ERR_UNSUPPORTED
