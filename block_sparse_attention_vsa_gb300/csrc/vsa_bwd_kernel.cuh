@@ -40,10 +40,12 @@
 //   warps 8-11  dQ warps: thread = d column (TMEM lane of dQ^T).
 //   warp 12     TMA: K, V once; per step Q, dO (64 rows) and lse, D (64 floats) into a
 //               3-stage ring.
-//   warp 13     MMA issuer (one thread) of S^T, dP^T, dV; owns the TMEM allocation.
+//   warp 13     MMA issuer of S^T, dP^T, dV; owns the TMEM allocation.
 //   warp 14     list: compacts the block-map column into the step list (in chunks);
-//               during the steps its lane 0 issues the dK and dQ^T MMAs (a second
-//               issuing thread: they depend on no other MMA of the step).
+//               during the steps it issues the dK and dQ^T MMAs (a second issuing
+//               thread: they depend on no other MMA of the step).
+//               Both issuing warps run their loops converged and the lane elect.sync
+//               picks issues (predicated, not branched): half the issue time per MMA.
 // TMEM (512 columns): two step slots (step g uses slot g & 1) at 0 and 128, each holding
 // S^T in its first 64 columns (P^T bf16 over 0-15 and 32-47) and dP^T in the next 64 (then
 // dQ^T of the same step, written over the consumed dP^T); dV 256-383, dK 384-511.  dS^T
@@ -373,16 +375,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
     } else if (warp == kMmaWarp) {
       // ---------------------------------------------------------------- MMA issue
-      if (lane == 0) {
+      // the whole warp runs the loop (waits voted), lane 0 alone issues
+      {
         constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);
         constexpr uint32_t kIdescG = idesc_bf16_f32(128, 128, false, true);
         const uint64_t k_kmaj = smem_desc_sw128(smem_addr(smem + kOffK), 16, 1024);
         const uint64_t v_kmaj = smem_desc_sw128(smem_addr(smem + kOffV), 16, 1024);
-        if (g0 == 0 && !wait(&ctl->kv_full, 0, ctl, a, 0x42)) ok = false;
+        if (g0 == 0 && !wait_warp(&ctl->kv_full, 0, ctl, a, 0x42)) ok = false;
         if (ok && a.stall) {
           // test hook: wait on a barrier no role ever completes, so the wait runs out,
           // the status word records code 0x5f and every role unwinds
-          wait(&ctl->never, 0, ctl, a, 0x5f);
+          wait_warp(&ctl->never, 0, ctl, a, 0x5f);
           ok = false;
         }
         // S^T (dP^T) of step gg into its slot: A = K (V) K-major, B = Q (dO) K-major,
@@ -396,18 +399,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 8; ++k) {
             const uint64_t oa = ((k >> 2) * (kKVTile / 2) + (k & 3) * 32) >> 4;
             const uint64_t ob = ((k >> 2) * (kQTile / 2) + (k & 3) * 32) >> 4;
-            mma_ss(tmem + kColSlot * b + (dp ? kColDPOff : 0u), ad + oa, bd + ob, kIdescS,
-                   k > 0 ? 1u : 0u);
+            warp_mma_ss(tmem + kColSlot * b + (dp ? kColDPOff : 0u), ad + oa, bd + ob, kIdescS,
+                        k > 0 ? 1u : 0u);
           }
-          mma_commit(dp ? &ctl->dp_full[b] : &ctl->s_full[b]);
+          warp_mma_commit(dp ? &ctl->dp_full[b] : &ctl->s_full[b]);
         };
         // the step's Q, dO have landed
         auto landed = [&](uint32_t gg) {
-          return wait(&ctl->ld_full[gg % kStages], (gg / kStages) & 1, ctl, a, 0x43);
+          return wait_warp(&ctl->ld_full[gg % kStages], (gg / kStages) & 1, ctl, a, 0x43);
         };
         // dP^T of step gg overwrites the slot's dQ^T of step gg - 2: read out by then
         auto dq_read = [&](uint32_t gg) {
-          return gg < 2 || wait(&ctl->dq_empty[gg & 1], ((gg - 2) >> 1) & 1, ctl, a, 0x47);
+          return gg < 2 || wait_warp(&ctl->dq_empty[gg & 1], ((gg - 2) >> 1) & 1, ctl, a, 0x47);
         };
         if (ok) {
           if (!landed(g0) || !dq_read(g0)) {
@@ -431,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_sd(gg + 1, false);
           }
           // dV += P^T dO: A = P^T (TMEM, 64 query columns as 32 packed), B = dO MN-major
-          if (!wait(&ctl->p_full[b], (gg >> 1) & 1, ctl, a, 0x44)) {
+          if (!wait_warp(&ctl->p_full[b], (gg >> 1) & 1, ctl, a, 0x44)) {
             ok = false;
             break;
           }
@@ -441,9 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t tS = tmem + kColSlot * b;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + kColDV, tS + 32 * (kk >> 1) + 8 * (kk & 1),
-                   do_mn + ((kk * 2048) >> 4), kIdescG, (gg > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&ctl->ld_empty[st]);  // this thread's readers of the stage are done
+            warp_mma_ts(tmem + kColDV, tS + 32 * (kk >> 1) + 8 * (kk & 1),
+                        do_mn + ((kk * 2048) >> 4), kIdescG, (gg > 0 || kk > 0) ? 1u : 0u);
+          warp_mma_commit(&ctl->ld_empty[st]);  // this thread's readers of the stage are done
           // dP^T of the next step into the other slot once its dQ^T (step gg - 1) is out
           if (i + 1 < n_steps) {
             if (!dq_read(gg + 1)) {
@@ -455,7 +458,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
     } else if (warp == kListWarp) {
       // ---------------------------------------------------------------- dK, dQ issue
       // The two contractions that take dS^T, on a second issuing thread: they depend on no
@@ -463,16 +465,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // step's 32 MMAs as fast as the tensor pipe runs them.
       //   dK  += dS^T Q    (A = dS^T K-major, B = Q MN-major, K = queries in 4 steps)
       //   dQ^T = K^T dS^T  (both MN-major, K = keys in 8 steps) over the step slot's dP^T
-      if (lane == 0) {
+      // (the whole warp runs the loop, lane 0 alone issues)
+      {
         constexpr uint32_t kIdescG = idesc_bf16_f32(128, 128, false, true);
         constexpr uint32_t kIdescQ = idesc_bf16_f32(128, 64, true, true);
         const uint64_t k_mn = smem_desc_sw128(smem_addr(smem + kOffK), kKVTile / 2, 1024);
-        if (g0 == 0 && !wait(&ctl->kv_full, 0, ctl, a, 0x51)) ok = false;
+        if (g0 == 0 && !wait_warp(&ctl->kv_full, 0, ctl, a, 0x51)) ok = false;
         for (int i = 0; i < n_steps && ok; ++i) {
           const uint32_t gg = g0 + i, db = gg & 1, st = gg % kStages;
           const uint64_t ds_mn = smem_desc_sw128(smem_addr(smem + kOffDS + db * kDSTile), 8192, 1024);
           const uint64_t ds_kmaj = smem_desc_sw128(smem_addr(smem + kOffDS + db * kDSTile), 16, 1024);
-          if (!wait(&ctl->ds_full[db], (gg >> 1) & 1, ctl, a, 0x52)) {
+          if (!wait_warp(&ctl->ds_full[db], (gg >> 1) & 1, ctl, a, 0x52)) {
             ok = false;
             break;
           }
@@ -481,18 +484,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               smem_desc_sw128(smem_addr(smem + kOffQ + st * kQTile), kQTile / 2, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tmem + kColDK, ds_kmaj + ((kk * 32) >> 4), q_mn + ((kk * 2048) >> 4),
-                   kIdescG, (gg > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&ctl->ld_empty[st]);  // this thread's readers of the stage are done
+            warp_mma_ss(tmem + kColDK, ds_kmaj + ((kk * 32) >> 4), q_mn + ((kk * 2048) >> 4),
+                        kIdescG, (gg > 0 || kk > 0) ? 1u : 0u);
+          warp_mma_commit(&ctl->ld_empty[st]);  // this thread's readers of the stage are done
           // dQ^T over the slot's dP^T, which the gradient warps have read (dS^T is ready)
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + kColSlot * db + kColDPOff, k_mn + ((k * 2048) >> 4),
-                   ds_mn + ((k * 2048) >> 4), kIdescQ, k > 0 ? 1u : 0u);
-          mma_commit(&ctl->dq_full[db]);
+            warp_mma_ss(tmem + kColSlot * db + kColDPOff, k_mn + ((k * 2048) >> 4),
+                        ds_mn + ((k * 2048) >> 4), kIdescQ, k > 0 ? 1u : 0u);
+          warp_mma_commit(&ctl->dq_full[db]);
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
     } else if (warp < 8) {
       // ---------------------------------------------------------------- P^T and dS^T
       const int wg = warp >> 2;
@@ -621,19 +623,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (dK takes the factor scale that dS^T left out)
   const bool any = g > 0;
   if (warp == kMmaWarp) {
-    if (lane == 0) {
-      if (any && ok) mma_commit(&ctl->acc_full);
-      // every MMA issued has completed before TMEM can be released
-      mma_commit(&ctl->drain);
-      wait(&ctl->drain, 0, ctl, a, 0x4c, true);
-    }
+    if (any && ok) warp_mma_commit(&ctl->acc_full);
+    // every MMA issued has completed before TMEM can be released
+    warp_mma_commit(&ctl->drain);
+    wait(&ctl->drain, 0, ctl, a, 0x4c, true);
     __syncwarp();
   } else if (warp == kListWarp) {
-    if (lane == 0) {  // every MMA this thread issued has completed before TMEM goes
-      if (any && ok) mma_commit(&ctl->acc_full_dk);
-      mma_commit(&ctl->drain_dq);
-      wait(&ctl->drain_dq, 0, ctl, a, 0x53, true);
-    }
+    // every MMA this warp issued has completed before TMEM goes
+    if (any && ok) warp_mma_commit(&ctl->acc_full_dk);
+    warp_mma_commit(&ctl->drain_dq);
+    wait(&ctl->drain_dq, 0, ctl, a, 0x53, true);
     __syncwarp();
   } else if (warp == kTmaWarp) {
     if (lane == 0) {  // every copy issued has landed before the CTA exits
