@@ -510,9 +510,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* nlse_s = reinterpret_cast<const float*>(smem + kOffRow + st * 512) + 32 * wg;
         const float* nD_s = nlse_s + 64;
         // -lse and -D of the step have landed (the stage is not refilled before dK of this
-        // step, which waits for this warp), and S^T is in TMEM
-        if (!wait_warp(&ctl->ld_full[st], (gg / kStages) & 1, ctl, a, 0x48) ||
-            !wait_warp(&ctl->s_full[b], (gg >> 1) & 1, ctl, a, 0x49)) {
+        // step, which waits for this warp); -lse is read into registers while S^T is still
+        // being computed
+        if (!wait_warp(&ctl->ld_full[st], (gg / kStages) & 1, ctl, a, 0x48)) {
+          ok = false;
+          break;
+        }
+        float4 l4[8];
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) l4[c4] = reinterpret_cast<const float4*>(nlse_s)[c4];
+        if (!wait_warp(&ctl->s_full[b], (gg >> 1) & 1, ctl, a, 0x49)) {
           ok = false;
           break;
         }
@@ -528,12 +535,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t c2 = f32x2(a.scale_log2, a.scale_log2);
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 l4 = reinterpret_cast<const float4*>(nlse_s)[c4];
             const int c = 4 * c4;
-            const uint64_t x01 = fma_f32x2(
-                f32x2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, f32x2(l4.x, l4.y));
+            const uint64_t x01 = fma_f32x2(f32x2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
+                                           c2, f32x2(l4[c4].x, l4[c4].y));
             const uint64_t x23 = fma_f32x2(
-                f32x2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), c2, f32x2(l4.z, l4.w));
+                f32x2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), c2,
+                f32x2(l4[c4].z, l4[c4].w));
             float x[4];
             split_f32x2(x01, x[0], x[1]);
             split_f32x2(x23, x[2], x[3]);
@@ -552,6 +559,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->p_full[b]);
+        float4 d4[8];  // -D, read while dP^T is still being computed
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) d4[c4] = reinterpret_cast<const float4*>(nD_s)[c4];
         if (!wait_warp(&ctl->dp_full[b], (gg >> 1) & 1, ctl, a, 0x4a)) {
           ok = false;
           break;
@@ -562,12 +572,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (valid) {  // dS = p (dP - D), without the factor scale
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 d4 = reinterpret_cast<const float4*>(nD_s)[c4];
             const int c = 4 * c4;
-            const uint64_t t01 = add_f32x2(
-                f32x2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), f32x2(d4.x, d4.y));
+            const uint64_t t01 = add_f32x2(f32x2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
+                                           f32x2(d4[c4].x, d4[c4].y));
             const uint64_t t23 = add_f32x2(
-                f32x2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), f32x2(d4.z, d4.w));
+                f32x2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])),
+                f32x2(d4[c4].z, d4[c4].w));
             split_f32x2(mul_f32x2(f32x2(p[c], p[c + 1]), t01), p[c], p[c + 1]);
             split_f32x2(mul_f32x2(f32x2(p[c + 2], p[c + 3]), t23), p[c + 2], p[c + 3]);
           }
