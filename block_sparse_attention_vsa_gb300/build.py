@@ -16,7 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libvsa_gb300.so")
 SOURCES = [os.path.join(CSRC, "vsa_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("vsa_fwd_kernel.cuh", "vsa_bwd_kernel.cuh", "sm103_ptx.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("vsa_fwd_kernel.cuh", "vsa_bwd_kernel.cuh", "vsa_bwd64_kernel.cuh",
+                                                "sm103_ptx.cuh")] + [
     os.path.join(ROOT, "include", "vsa.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

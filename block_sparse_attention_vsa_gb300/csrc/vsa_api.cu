@@ -15,6 +15,7 @@
 
 #include "../../include/vsa.h"
 #include "vsa_fwd_kernel.cuh"
+#include "vsa_bwd64_kernel.cuh"
 #include "vsa_bwd_kernel.cuh"
 
 namespace vsa {
@@ -135,15 +136,16 @@ bool make_map(CUtensorMap* m, const void* ptr, long long rows, int box_rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D view [heads, seq, 128] of a BHSD bf16 tensor, box {64, 128, 1}: a box that runs
+// 3-D view [heads, seq, 128] of a BHSD bf16 tensor, box {64, box_rows, 1}: a box that runs
 // past the end of a head's sequence is clipped there (loads read zeros, stores drop the
 // rows) instead of spilling into the next head.
-bool make_map_3d(CUtensorMap* m, const void* ptr, long long heads, long long seq) {
+bool make_map_3d(CUtensorMap* m, const void* ptr, long long heads, long long seq,
+                 int box_rows = 128) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {128, (cuuint64_t)seq, (cuuint64_t)heads};
   cuuint64_t strides[2] = {128 * 2, (cuuint64_t)seq * 128 * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -405,6 +407,30 @@ vsa_status launch_bwd(DeviceInfo* dev, const BwdArgs& a, const void* q, const vo
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
+// The block-64 backward: one CTA per key block, Q/dO in 64-row boxes (one list entry),
+// K/V in 64-row boxes.
+vsa_status launch_bwd64(DeviceInfo* dev, const BwdArgs& a, const void* q, const void* k,
+                        const void* v, const void* dout, long long rows_q, long long kv_heads,
+                        long long n_ctas, cudaStream_t s) {
+  auto kern = bwd64::bsa_bwd64_kernel;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!dev->bwd_attr_set[0]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)bwd64::kSmemBytes) != cudaSuccess)
+        return VSA_ERR_CUDA;
+      dev->bwd_attr_set[0] = true;
+    }
+  }
+  if (n_ctas == 0) return VSA_OK;
+  CUtensorMap tq, tdo, tk, tv;
+  if (!make_map(&tq, q, rows_q, 64) || !make_map(&tdo, dout, rows_q, 64) ||
+      !make_map_3d(&tk, k, kv_heads, a.Sk, 64) || !make_map_3d(&tv, v, kv_heads, a.Sk, 64))
+    return VSA_ERR_CUDA;
+  kern<<<(unsigned)n_ctas, bwd64::kThreads, bwd64::kSmemBytes, s>>>(tq, tdo, tk, tv, a);
+  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
+}
+
 // Streams and events of vsa_fwd_from_host, created once per device (no device memory).
 constexpr int kHostChunks = 8;
 struct HostPipe {
@@ -537,13 +563,13 @@ vsa_status vsa_bwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
   a.Sk = Sk;
   a.nbq = nbq;
   a.nbk = nbk;
-  a.n_tiles = block == 64 ? (nbk + 1) / 2 : nbk;  // key tiles of 128 keys per head
+  a.n_tiles = nbk;  // block 128: one key tile per key block
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_ns = launch_wait_ns(bwd::kWaitLimitNs);
   a.stall = g_stall.load();
-  const long long n_ctas = (long long)B * Hkv * a.n_tiles;
-  st = block == 64 ? launch_bwd<64>(dev, a, q, k, v, dout, rows, (long long)B * Hkv, n_ctas, s)
+  const long long n_ctas = (long long)B * Hkv * nbk;  // one CTA per key block
+  st = block == 64 ? launch_bwd64(dev, a, q, k, v, dout, rows, (long long)B * Hkv, n_ctas, s)
                    : launch_bwd<128>(dev, a, q, k, v, dout, rows, (long long)B * Hkv, n_ctas, s);
   if (st != VSA_OK) return st;
   if (n_ctas > 0) ++launches;

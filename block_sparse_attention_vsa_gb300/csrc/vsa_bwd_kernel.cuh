@@ -180,7 +180,9 @@ static_assert(kSmemBytes <= 227 * 1024, "backward SMEM");
 // limit a.wait_ns, recording `code` in the status word and raising the abort flag, or as
 // soon as another role has raised the flag -- unless `drain`, for copies / MMAs still in
 // flight, which always runs to the full kWaitLimitNs.
-__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, Ctl* ctl, const BwdArgs& a,
+// (The control block type is a parameter: both backward kernels use these waits.)
+template <class CtlT>
+__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, CtlT* ctl, const BwdArgs& a,
                                      unsigned code, bool drain = false) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t limit = drain ? kWaitLimitNs : a.wait_ns;
@@ -199,7 +201,8 @@ __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, Ctl* ctl, c
 // The same wait by every lane of a warp that goes on to warp-collective TMEM accesses: the
 // warp proceeds only if every lane saw the phase complete, so an abort can never leave
 // part of a warp inside a .sync.aligned instruction.
-__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Ctl* ctl,
+template <class CtlT>
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, CtlT* ctl,
                                           const BwdArgs& a, unsigned code) {
   const bool w = wait(bar, parity, ctl, a, code);
   return __all_sync(0xffffffffu, w);
