@@ -382,23 +382,23 @@ BwdLayout bwd_layout(long long B, long long Hq, long long Sq, long long Sk, int 
   return l;
 }
 
-template <int BLOCK>
-vsa_status launch_bwd(DeviceInfo* dev, const BwdArgs& a, const void* q, const void* k,
-                      const void* v, const void* dout, long long rows_q, long long kv_heads,
-                      long long n_ctas, cudaStream_t s) {
-  auto kern = bwd::bsa_bwd_kernel<BLOCK>;
+// The block-128 backward: one CTA per key block.
+vsa_status launch_bwd128(DeviceInfo* dev, const BwdArgs& a, const void* q, const void* k,
+                         const void* v, const void* dout, long long rows_q, long long kv_heads,
+                         long long n_ctas, cudaStream_t s) {
+  auto kern = bwd::bsa_bwd_kernel;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!dev->bwd_attr_set[BLOCK == 128]) {
+    if (!dev->bwd_attr_set[1]) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)bwd::kSmemBytes) != cudaSuccess)
         return VSA_ERR_CUDA;
-      dev->bwd_attr_set[BLOCK == 128] = true;
+      dev->bwd_attr_set[1] = true;
     }
   }
   if (n_ctas == 0) return VSA_OK;
   // Q and dO: [rows, 128] with 64-row boxes (a step); K and V: [heads, Sk, 128] with
-  // 128-row boxes clipped at the end of a head (a lone last block-64 key block)
+  // 128-row boxes (a key block)
   CUtensorMap tq, tdo, tk, tv;
   if (!make_map(&tq, q, rows_q, 64) || !make_map(&tdo, dout, rows_q, 64) ||
       !make_map_3d(&tk, k, kv_heads, a.Sk) || !make_map_3d(&tv, v, kv_heads, a.Sk))
@@ -563,14 +563,13 @@ vsa_status vsa_bwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
   a.Sk = Sk;
   a.nbq = nbq;
   a.nbk = nbk;
-  a.n_tiles = nbk;  // block 128: one key tile per key block
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_ns = launch_wait_ns(bwd::kWaitLimitNs);
   a.stall = g_stall.load();
   const long long n_ctas = (long long)B * Hkv * nbk;  // one CTA per key block
   st = block == 64 ? launch_bwd64(dev, a, q, k, v, dout, rows, (long long)B * Hkv, n_ctas, s)
-                   : launch_bwd<128>(dev, a, q, k, v, dout, rows, (long long)B * Hkv, n_ctas, s);
+                   : launch_bwd128(dev, a, q, k, v, dout, rows, (long long)B * Hkv, n_ctas, s);
   if (st != VSA_OK) return st;
   if (n_ctas > 0) ++launches;
   const long long n8 = rows * 16;
