@@ -462,7 +462,8 @@ def main():
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": TRAFFIC.get(w.name),
                 "peak_source": f"{peak_src} dense bf16 (burst)",
-                "kernel": "bsa_bwd_kernel (whole vsa_bwd call timed)" if bwd else "bsa_fwd_kernel"}
+                "kernel": (("bsa_bwd64_kernel" if w.block == 64 else "bsa_bwd_kernel") +
+                           " (whole vsa_bwd call timed)") if bwd else "bsa_fwd_kernel"}
     if bwd:
         roofline["traffic"] = TRAFFIC_BWD.get(w.name)
 
@@ -509,8 +510,9 @@ def main():
 # same kernel build on the same workload; absent = not measured for the current kernel.
 TRAFFIC = {"vsa_long_video": 2462.8e6,  # captured on 4 of 24 heads, scaled by 6
            "jenga": 385.2e6, "vsa_mid": 183.6e6, "vsa_blk128": 1609.1e6}
-# the same for the backward kernel (bsa_bwd_kernel), per launch
-TRAFFIC_BWD = {"vsa_mid": 456.4e6}
+# the same for the backward kernel (bsa_bwd64_kernel for block 64, bsa_bwd_kernel for 128)
+TRAFFIC_BWD = {"vsa_mid": 460.8e6,
+               "vsa_blk128": 3913.3e6}  # captured on 8 of 24 heads, scaled by 3
 
 
 if __name__ == "__main__":
