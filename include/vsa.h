@@ -277,10 +277,10 @@ VSA_API vsa_status vsa_bitmap_to_lut(const int8_t *bitmap, int rows, int nb, int
 /* vsa_fwd with HOST buffers: copies q, k, v, q2k_idx, q2k_num, variable_block_sizes
  * from host memory into the caller's device buffers (the d_* arguments, same shapes as
  * vsa_fwd), runs the forward, and copies out (and lse, if h_lse is not NULL) back to host
- * memory.  The work is split into up to 8 chunks of consecutive (b, h) heads: a chunk's
- * inputs go over on an input stream, its forward runs on `stream` as soon as they have
- * landed, and its outputs come back on an output stream, so copies of one chunk overlap
- * the forward of another.  The two internal streams (and their events) are created once
+ * memory.  The work is split into chunks of consecutive (b, h) heads (about 20 MB of q,
+ * k, v each, at most 32, at most one per head): a chunk's inputs go over on an input
+ * stream, its forward runs on `stream` as soon as they have landed, and its outputs come
+ * back on an output stream, so copies of one chunk overlap the forward of another.  The two internal streams (and their events) are created once
  * per device on first use -- no device memory -- and fork from `stream` at the start of
  * the call and join it at the end: everything is ordered after earlier work on `stream`,
  * and later work on `stream` (or a synchronisation of it) sees the whole call complete.

@@ -218,18 +218,28 @@ def test_from_host_buffers():
     assert torch.equal(h_out, ref_out.cpu()) and torch.equal(h_lse, ref_lse.cpu())
 
 
-@pytest.mark.parametrize("block,B,H,with_lse,dynamic", [(64, 2, 5, True, False),
-                                                          (128, 1, 3, False, True),
-                                                          (64, 1, 11, True, True)])
-def test_from_host_chunks_on_a_side_stream(block, B, H, with_lse, dynamic):
-    """The host-buffer entry splits the heads into up to 8 chunks (uneven ones included)
-    whose copies overlap other chunks' forwards on internal streams forked from the caller's
-    stream; the result equals vsa_fwd's bit for bit and the oracle's within tolerance, and
-    work enqueued on the caller's stream afterwards sees the copies complete."""
-    w = small(block, 23 + H, B=B, H=H)
+def host_chunks(B, H, S):
+    """Chunks vsa_fwd_from_host makes: about 20 MB of q, k, v each, at most 32, at most one
+    per (b, h) head."""
+    n = -(-(B * H * 3 * S * 128 * 2) // (20 << 20))
+    return min(max(1, min(32, n)), B * H)
+
+
+@pytest.mark.parametrize("block,B,H,nbk,with_lse,dynamic", [(64, 2, 5, 16, True, False),
+                                                              (128, 1, 3, 16, False, True),
+                                                              (64, 1, 11, 128, True, True),
+                                                              (128, 2, 7, 64, True, False)])
+def test_from_host_chunks_on_a_side_stream(block, B, H, nbk, with_lse, dynamic):
+    """The host-buffer entry splits the heads into chunks (uneven ones included: the two
+    larger cases make 4 and 5 chunks of 11 and 14 heads) whose copies overlap other chunks'
+    forwards on internal streams forked from the caller's stream; the result equals
+    vsa_fwd's bit for bit (and, on the small cases, the oracle's within tolerance), and work
+    enqueued on the caller's stream afterwards sees the copies complete."""
+    w = small(block, 23 + H, B=B, H=H, nbk=nbk)
     dev = to_dev(w)
     ref_out, ref_lse = run_gpu(w, dev)
-    compare(w, ref_out, ref_lse)
+    if nbk <= 16:
+        compare(w, ref_out, ref_lse)
     h = dict(q=w.q.pin_memory(), k=w.k.pin_memory(), v=w.v.pin_memory(),
              idx=torch.from_numpy(w.q2k_idx).pin_memory(),
              num=torch.from_numpy(w.q2k_num).pin_memory(),
@@ -249,7 +259,7 @@ def test_from_host_chunks_on_a_side_stream(block, B, H, with_lse, dynamic):
         # enqueued after the call on the same stream: must see every chunk's copy done
         probe = bufs["out"].float().sum()
     side.synchronize()
-    assert binding.vsa_last_launch_count() == min(8, B * H)
+    assert binding.vsa_last_launch_count() == host_chunks(B, H, w.S)
     assert torch.equal(h_out, ref_out.cpu())
     assert torch.equal(bufs["q"], dev["q"]) and torch.equal(bufs["idx"], dev["idx"])
     assert probe.item() == ref_out.float().sum().item()
@@ -257,6 +267,15 @@ def test_from_host_chunks_on_a_side_stream(block, B, H, with_lse, dynamic):
         assert torch.equal(h_lse, ref_lse.cpu())
     code, detail = binding.vsa_device_status()
     assert code == binding.VSA_OK, hex(detail)
+
+
+def test_host_chunk_counts():
+    """The chunk rule on the benchmark shapes: one-head chunks for B1 H24 S98304, eight for
+    B1 H12 S16384, the cap of 32 for B2 H24 S32768."""
+    assert host_chunks(1, 24, 98304) == 24
+    assert host_chunks(1, 12, 16384) == 8
+    assert host_chunks(2, 24, 32768) == 32
+    assert host_chunks(1, 11, 8192) == 4 and host_chunks(2, 7, 8192) == 5
 
 
 # ------------------------------------------------------------- metadata conversions
