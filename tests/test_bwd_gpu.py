@@ -108,12 +108,35 @@ def test_backward_larger_case():
 
 def test_backward_column_longer_than_one_list_chunk():
     # 8 query heads share one key/value head and all 512 query blocks of each select key
-    # blocks 0 and 1: 4096 (head, query block) pairs select the first key tile, more than
-    # one 2048-entry list chunk
+    # blocks 0 and 1: 4096 (head, query block) pairs select each of them, more than one
+    # 2048-entry list chunk
     w = workloads.make_random_gqa(1, 8, 1, 512 * 64, 4 * 64, 128, 64, 2, seed=135, n_lo=2)
     w.q2k_idx[..., 0] = 0
     w.q2k_idx[..., 1] = 1
     run_and_compare(w)
+
+
+@pytest.mark.parametrize("block", [64, 128])
+def test_backward_odd_column_lengths(block):
+    """Key blocks selected by 1, 3, 0 and 5 query blocks (of 6, two query heads sharing a
+    key/value head, so 2, 6, 0, 10 entries; and 1, 3, 0, 5 with one head): with block 64 a
+    step takes two entries, so an odd column ends in a step whose second half is padding;
+    a key block nobody selects gets dk = dv = 0."""
+    for hq in (1, 2):
+        w = workloads.make_random_gqa(1, hq, 1, 6 * block, 4 * block, 128, block, 4,
+                                      seed=140 + hq, vbs_lo=block // 2, vbs_hi=block)
+        sel = {0: [2], 1: [0, 3, 5], 2: [], 3: [0, 1, 2, 4, 5]}
+        w.q2k_idx[...] = -1
+        w.q2k_num[...] = 0
+        for kb, qbs in sel.items():
+            for qb in qbs:
+                for h in range(hq):
+                    n = w.q2k_num[0, h, qb]
+                    w.q2k_idx[0, h, qb, n] = kb
+                    w.q2k_num[0, h, qb] = n + 1
+        dq, dk, dv = run_and_compare(w)
+        rows = slice(2 * block, 3 * block)
+        assert not dk[0, 0, rows].float().abs().any() and not dv[0, 0, rows].float().abs().any()
 
 
 def _sampled_full_size(w, samples):
@@ -179,7 +202,7 @@ def _sampled_full_size(w, samples):
 
 
 def test_mid_workload_sampled_full_size():
-    # vsa_mid: both blocks of a key tile, the first and last tiles, several heads
+    # vsa_mid: the first and last key blocks, neighbouring ones, several heads
     w = workloads.make("vsa_mid")
     _sampled_full_size(w, [(0, 0, 0), (0, 0, 255), (0, 5, 128), (0, 11, 63), (0, 3, 1),
                            (0, 7, 200)])
