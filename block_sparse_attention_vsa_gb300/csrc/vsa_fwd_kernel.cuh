@@ -37,8 +37,10 @@
 //               allowed to lag the true max by up to 2^32 before O and l are rescaled),
 //               row sums and O accumulator, so the two never synchronise inside the key
 //               loop.  After the item they merge (m, l, O) of both halves and each
-//               warpgroup normalises, stages and TMA-stores one 64-column half of the
-//               output; warpgroup 0 writes lse.
+//               warpgroup normalises, stages (in the item's Q buffer) and TMA-stores
+//               one 64-column half of the output; warpgroup 0 writes lse.  The store
+//               leader releases that Q buffer only after the next item's first tile,
+//               so the store's read of SMEM never holds up an item boundary.
 //   warp 11     idle.
 // TMEM (512 columns): S0, S1 at columns 0, 128 (warpgroup w reads S columns 64w..64w+63
 // and writes its bf16 P over the first 32 of them); O0, O1 at 256, 384.
@@ -89,6 +91,9 @@ constexpr unsigned kErrTimeout = 0x100u;  // | code of the wait that gave up
 
 struct SmemCtl {
   uint64_t list_full[2], list_empty[2];
+  // q_full[b]: Q of an item landed in buffer b.  q_empty[b]: both store leaders' output
+  // stores have read buffer b (the output is staged in the item's Q buffer), arrived one
+  // tile into the next item, so the TMA warp can load the item after next.
   uint64_t q_full[2], q_empty[2];
   // kv_full[s]: ring stage s holds its tile.  kv_empty[s]: the MMAs that read the
   // stage's tile have completed.  The MMA warp commits kv_empty right after a tile's QK
@@ -623,6 +628,8 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
   uint32_t g = 0;         // key tiles seen so far, across items (S buffer g & 1)
   uint32_t ring = 0;      // ring position of the current item's first K tile
   uint32_t ne_items = 0;
+  bool have_prev = false;  // store leader: an item's store whose Q buffer is not yet released
+  uint32_t prev_buf = 0;
   for (uint32_t it = 0;; ++it) {
     const uint32_t buf = it & 1;
     if (!wait_warp(&ctl->list_full[buf], (it >> 1) & 1, ctl, a, 20)) break;
@@ -696,6 +703,11 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
       __syncwarp();
       if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->p_full[sb]);
       started = true;
+      if (leader && have_prev) {  // the previous item's store has had a tile to read
+        bulk_wait_group_read0();
+        mbar_arrive(&ctl->q_empty[prev_buf]);
+        have_prev = false;
+      }
     }
     if (!ok) break;
     ring += 2u * (uint32_t)n_tiles;  // the item's K and V tiles
@@ -794,15 +806,22 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
     const bool stored = !leader || wait_bar(&ctl->epi_bar[w], it & 1, ctl, a, 24);
     if (!__all_sync(0xffffffffu, stored)) break;
     if (leader) {
+      if (have_prev) {  // an item without tiles in between: release the older buffer now
+        bulk_wait_group_read0();
+        mbar_arrive(&ctl->q_empty[prev_buf]);
+      }
       if (!split) {
         tma_store_3d(to, qs, w * 64, qa * BLOCK, bh);  // rows past Sq are not written
         bulk_commit_group();
-        bulk_wait_group_read0();
       }
-      mbar_arrive(&ctl->q_empty[buf]);
+      have_prev = true;
+      prev_buf = buf;
     }
   }
-  if (leader) bulk_wait_group0();
+  if (leader) {
+    bulk_wait_group0();
+    if (have_prev) mbar_arrive(&ctl->q_empty[prev_buf]);
+  }
 }
 
 // ------------------------------------------------------------------------------------
