@@ -120,10 +120,12 @@ def test_forward_short_limit_gives_up_mid_pipeline(hooks):
     assert timeouts >= 1
 
 
-def test_backward_stall_reports_timeout(hooks):
+@pytest.mark.parametrize("block", [64, 128])
+def test_backward_stall_reports_timeout(hooks, block):
+    """Both backward kernels (one per block size) unwind from a stalled MMA warp."""
     from block_sparse_attention_vsa_gb300 import workloads
     binding = hooks
-    w = workloads.make_random_vsa(1, 2, 8 * 64, 128, 64, 4, seed=47, n_lo=1)
+    w = workloads.make_random_vsa(1, 2, 8 * block, 128, block, 4, seed=47, n_lo=1)
     dev = gpu_util.to_dev(w)
     out, lse = binding.vsa_fwd(dev["q"], dev["k"], dev["v"], dev["idx"], dev["num"], dev["vbs"],
                                block=w.block, scale=w.scale)
