@@ -154,3 +154,44 @@ def test_backward_stall_reports_timeout(hooks, block):
     for got, ref in zip((dq, dk, dv), refs):
         e = np.abs(got.float().cpu().numpy().astype(np.float64) - ref)
         assert e.max() <= 2e-2 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("block", [64, 128])
+def test_backward_short_limit_gives_up_mid_pipeline(hooks, block):
+    """A 1 ns limit on the backward's non-drain waits: they give up while copies and MMAs
+    are in flight (the drains keep their full limit).  At least one of the launches must
+    report the timeout, and each is followed by a clean backward that matches the oracle."""
+    from block_sparse_attention_vsa_gb300 import workloads
+    from oracle import oracle as orc
+    binding = hooks
+    timeouts = 0
+    for seed in (61, 62, 63):
+        w = workloads.make_random_vsa(1, 4, 16 * block, 128, block, 8, seed=seed, n_lo=2)
+        dev = gpu_util.to_dev(w)
+        out, lse = binding.vsa_fwd(dev["q"], dev["k"], dev["v"], dev["idx"], dev["num"],
+                                   dev["vbs"], block=w.block, scale=w.scale)
+        g = torch.Generator().manual_seed(seed)
+        dout_cpu = torch.randn(w.q.shape, generator=g).to(torch.bfloat16)
+        dout = dout_cpu.to(dev["q"].device)
+        binding.vsa_set_wait_limit_ns(1)
+        binding.vsa_bwd(dev["q"], dev["k"], dev["v"], out, dout, lse, dev["idx"], dev["num"],
+                        dev["vbs"], block=w.block, scale=w.scale)
+        torch.cuda.synchronize()
+        code, detail = binding.vsa_device_status()
+        binding.vsa_set_wait_limit_ns(0)
+        assert code in (binding.VSA_OK, binding.VSA_ERR_DEVICE_TIMEOUT), code
+        if code == binding.VSA_ERR_DEVICE_TIMEOUT:
+            assert detail & 0xF00 == 0x100, hex(detail)
+            timeouts += 1
+        dq, dk, dv = binding.vsa_bwd(dev["q"], dev["k"], dev["v"], out, dout, lse, dev["idx"],
+                                     dev["num"], dev["vbs"], block=w.block, scale=w.scale)
+        torch.cuda.synchronize()
+        code, detail = binding.vsa_device_status()
+        assert code == binding.VSA_OK, hex(detail)
+        refs = orc.vsa_backward(workloads.bits(w.q), workloads.bits(w.k), workloads.bits(w.v),
+                                workloads.bits(dout_cpu), w.q2k_idx, w.q2k_num, w.vbs, w.block,
+                                w.scale)
+        for got, ref in zip((dq, dk, dv), refs):
+            e = np.abs(got.float().cpu().numpy().astype(np.float64) - ref)
+            assert e.max() <= 2e-2 * np.abs(ref).max()
+    assert timeouts >= 1
