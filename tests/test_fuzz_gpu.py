@@ -1,7 +1,8 @@
 """Randomised parity sweep: seeded random small configurations through the forward (LUT or
-grouped-head route, every third case also split-KV) and the backward, each compared with the
-oracle at the contract's tolerances (gpu_util for the forward; the backward bounds of
-test_bwd_gpu.py).
+grouped-head route, every third case also split-KV) and the backward, and through the two
+block-map routes (a shared Jenga bitmap, a per-head map for vsa_fwd_from_mask), each compared
+with the oracle at the contract's tolerances (gpu_util for the forward; the backward bounds
+of test_bwd_gpu.py).
 
 A case draws the block size (64 or 128), 1-2 batches, 1-2 key/value heads with 1-3 query
 heads each, 1-8 query blocks, 1-10 key blocks (so Sq and Sk differ, and a block-64 head can
@@ -95,3 +96,42 @@ def test_random_case(seed):
         out_s, lse_s = run_gpu(w, dev, workspace=ws, splits=splits)
         compare(w, out_s, lse_s)
     backward_compare(w, dev, out, lse, seed)
+
+
+def random_mask_case(seed):
+    """A block-map case: even seeds a Jenga map shared by every head (square, no grouping, no
+    tail masks), odd seeds a per-head int8 map for vsa_fwd_from_mask (grouped heads, cross
+    length, tail masks).  Density is drawn per case; selected bytes take any nonzero value."""
+    rng = np.random.default_rng(8000 + seed)
+    block = int(rng.choice([64, 128]))
+    B = int(rng.integers(1, 3))
+    jenga = seed % 2 == 0
+    if jenga:
+        Hkv = Hq = int(rng.integers(1, 4))
+        nbq = nbk = int(rng.integers(1, 10))
+    else:
+        Hkv = int(rng.integers(1, 3))
+        Hq = Hkv * int(rng.integers(1, 4))
+        nbq, nbk = int(rng.integers(1, 9)), int(rng.integers(1, 11))
+    qk_mul = 3.0 if rng.random() < 0.25 else 1.0
+    w = workloads.make_random_gqa(B, Hq, Hkv, nbq * block, nbk * block, 128, block, nbk,
+                                  seed=9500 + seed, vbs_lo=None if jenga else 0,
+                                  vbs_hi=None if jenga else block, kind="mask",
+                                  shared_map=jenga, qk_mul=qk_mul)
+    shape = (nbq, nbk) if jenga else (B, Hq, nbq, nbk)
+    values = rng.integers(-128, 128, size=shape).astype(np.int8)
+    values[values == 0] = 1
+    bm = np.where(rng.random(shape) < rng.uniform(0.0, 1.0), values, 0).astype(np.int8)
+    if jenga:
+        return workloads.Workload(name="jenga_random", kind="jenga", B=B, H=Hq, S=w.S, D=w.D,
+                                  block=block, scale=w.scale, q=w.q, k=w.k, v=w.v,
+                                  bitmap=np.ascontiguousarray(bm))
+    w.block_map = np.ascontiguousarray(bm)
+    return w
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_mask_case(seed):
+    w = random_mask_case(seed)
+    out, lse = run_gpu(w, to_dev(w))
+    compare(w, out, lse)
