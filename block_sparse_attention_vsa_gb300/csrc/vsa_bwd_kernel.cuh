@@ -28,7 +28,7 @@
 //                       dK  += dS^T Q     (A = dS^T K-major in SMEM, B = Q MN-major)
 //                       dQ^T = K^T dS^T   (both operands MN-major in SMEM; M = 128 d)
 //                     and the dQ warps add dQ^T (one thread per d column, 64 query rows)
-//                     into an fp32 accumulator with coalesced reductions: several key tiles
+//                     into an fp32 accumulator with coalesced reductions: several key blocks
 //                     feed every query row.
 //   bwd_dq_kernel     fp32 dQ accumulator times scale -> bf16 dq.
 //
@@ -37,7 +37,7 @@
 //               thread = key row (TMEM lane); after the last step they store dV (warps
 //               0-3) and dK (warps 4-7) as bf16.
 //   warps 8-11  dQ warps: thread = d column (TMEM lane of dQ^T).
-//   warp 12     TMA: K, V once; per step Q, dO (64 rows) and lse, D (64 floats) into a
+//   warp 12     TMA: K, V once; per step Q, dO (64 rows) and -lse, -D (64 floats) into a
 //               3-stage ring.
 //   warp 13     MMA issuer of S^T, dP^T, dV; owns the TMEM allocation.
 //   warp 14     list: compacts the block-map column into the step list (in chunks);
