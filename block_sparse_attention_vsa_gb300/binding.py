@@ -241,14 +241,15 @@ def new_split_workspace(B, Hq, Sq, block, num_splits, device=None) -> torch.Tens
 
 
 def default_splits(B, Hq, Sq, block, sm_count) -> int:
-    """Ranges per item so that about one unit per SM exists (1 when the items already fill
-    the SMs).  Finer ranges measured slower: each range pays a Q load, a pipeline fill and
-    a 64 KB partial."""
+    """Ranges per item: the most that still give every (item, range) unit its own SM (1 when
+    the items already fill the SMs).  One more range than that puts a few units in a second
+    wave (24 heads x 98,304 keys: 6 ranges 88 us, 7 ranges 111 us), and finer ranges measured
+    slower: each range pays a Q load, a pipeline fill and a 64 KB partial."""
     nbq = Sq // block
     items = B * Hq * ((nbq + 1) // 2 if block == 64 else nbq)
     if items == 0 or items >= sm_count:
         return 1
-    return max(1, min(MAX_SPLITS, -(-sm_count // items)))
+    return max(1, min(MAX_SPLITS, sm_count // items))
 
 
 def vsa_fwd_split(q, k, v, q2k_idx, q2k_num, variable_block_sizes=None, block=64, scale=None,
