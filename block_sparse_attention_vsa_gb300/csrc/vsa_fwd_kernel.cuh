@@ -102,9 +102,10 @@ struct SmemCtl {
   // every kStages ring positions, and the tile loaded there next cannot be consumed
   // before every waiter has moved on, so no waiter is ever two phases behind.
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t p_full[2];   // all 8 softmax warps have written P into S buffer b (per buffer,
-                        // so a warp running a tile ahead can never complete the previous
-                        // tile's phase)
+  uint64_t p_full[4];   // [2 b + w]: the 4 warps of softmax warpgroup w have written their
+                        // P into S buffer b (per buffer, so a warp running a tile ahead can
+                        // never complete the previous tile's phase; per warpgroup, so each
+                        // key half's PV starts as soon as its own P is there)
   uint64_t o_full, o_empty;
   uint64_t stats_bar[2];
   uint64_t epi_bar[2];
@@ -516,14 +517,17 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
             smem_desc_sw128(smem_addr(smem + kOffKV + stage * kTileBytes), kTileBytes / 2, 1024);
         const uint32_t pb = (g + tp) & 1;
         const uint32_t tS = tmem + kColS + pb * 128;
-        if (!wait_bar(&ctl->p_full[pb], ((g + tp) >> 1) & 1, ctl, a, 14)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        bool pw = true;
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
-          if (w >= halves) break;
+          // this half's warpgroup has written its P (both are waited, so every phase of
+          // both barriers is consumed, even for a 64-key tile)
+          if (!wait_bar(&ctl->p_full[pb * 2 + w], ((g + tp) >> 1) & 1, ctl, a, 14)) {
+            pw = false;
+            break;
+          }
+          tc_fence_after();
+          if (w >= halves) continue;
           const uint32_t tO = tmem + kColO + w * 128;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -531,6 +535,10 @@ __device__ void mma_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint32_t
                    (!first[w] || k > 0) ? 1u : 0u);
           }
           first[w] = false;
+        }
+        if (!pw) {
+          ok = false;
+          break;
         }
         mma_commit(&ctl->kv_empty[stage]);  // V stage free; O holds this tile
         ++L;
@@ -647,7 +655,7 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
       const int e0 = t * C::kSub;
       const int ne = (count - e0) < C::kSub ? (count - e0) : C::kSub;
       // A 64-key tile has no second half: warpgroup 1 then writes nothing, but still
-      // waits for the tile and arrives, so that every P phase takes all 8 warps.
+      // waits for the tile and arrives, so that every phase of both P barriers completes.
       const bool has_half = ne * BLOCK / 64 > w;
       int lim = 0;
       if (has_half) {
@@ -701,7 +709,7 @@ __device__ void softmax_role(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, uint
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->p_full[sb]);
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->p_full[sb * 2 + w]);
       started = true;
       if (leader && have_prev) {  // the previous item's store has had a tile to read
         bulk_wait_group_read0();
@@ -841,7 +849,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->list_empty[i], 10);  // the TMA warp, the MMA thread, 8 softmax warps
       mbar_init(&ctl->q_full[i], 1);
       mbar_init(&ctl->q_empty[i], 2);     // one TMA-store leader per softmax warpgroup
-      mbar_init(&ctl->p_full[i], 8);
+      mbar_init(&ctl->p_full[i], 4);
+      mbar_init(&ctl->p_full[i + 2], 4);
       mbar_init(&ctl->stats_bar[i], 8);
       mbar_init(&ctl->epi_bar[i], 4);
     }
