@@ -508,8 +508,8 @@ def main():
 
 # DRAM bytes (read + write) per launch of the forward kernel, from an ncu capture of the
 # same kernel build on the same workload; absent = not measured for the current kernel.
-TRAFFIC = {"vsa_long_video": 2462.1e6,  # captured on 4 of 24 heads, scaled by 6
-           "jenga": 385.5e6, "vsa_mid": 183.1e6, "vsa_blk128": 1610.3e6}
+TRAFFIC = {"vsa_long_video": 2473.4e6,  # captured on 4 of 24 heads, scaled by 6
+           "jenga": 385.7e6, "vsa_mid": 183.4e6, "vsa_blk128": 1610.9e6}
 # the same for the backward kernel (bsa_bwd64_kernel for block 64, bsa_bwd_kernel for 128)
 TRAFFIC_BWD = {"vsa_mid": 460.8e6,
                "vsa_blk128": 3913.3e6}  # captured on 8 of 24 heads, scaled by 3
