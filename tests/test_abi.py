@@ -150,6 +150,21 @@ def test_split_validation(lib):
     assert lib.vsa_split_workspace_bytes(1, 2, 256, 64, 0) == 0
 
 
+def test_default_splits_fill_one_wave():
+    """Split-KV ranges per item: the most that still give every (item, range) unit its own
+    SM, 1 once the items fill the SMs, at most MAX_SPLITS."""
+    # 24 heads of 128 query rows (one block-64 pair each) on 152 SMs: 6 ranges, 144 units
+    assert binding.default_splits(1, 24, 128, 64, 152) == 6
+    # block 128: one item per query block, 16 items
+    assert binding.default_splits(2, 4, 256, 128, 152) == 9
+    # the items already fill the SMs
+    assert binding.default_splits(1, 152, 128, 64, 152) == 1
+    assert binding.default_splits(1, 12, 16384, 64, 152) == 1
+    # one item
+    assert binding.default_splits(1, 1, 128, 64, 152) == binding.MAX_SPLITS
+    assert binding.default_splits(1, 0, 128, 64, 152) == 1
+
+
 def _bwd(lib, ws_bytes=1 << 30, **kw):
     P = ctypes.c_void_p
     args = dict(B=1, Hq=2, Hkv=1, Sq=256, Sk=512, D=128, block=64, max_kv=4)
