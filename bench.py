@@ -512,7 +512,8 @@ TRAFFIC = {"vsa_long_video": 2473.4e6,  # captured on 4 of 24 heads, scaled by 6
            "jenga": 385.7e6, "vsa_mid": 183.4e6, "vsa_blk128": 1610.9e6}
 # the same for the backward kernel (bsa_bwd64_kernel for block 64, bsa_bwd_kernel for 128)
 TRAFFIC_BWD = {"vsa_mid": 460.8e6,
-               "vsa_blk128": 3913.3e6}  # captured on 8 of 24 heads, scaled by 3
+               "vsa_blk128": 3913.3e6,  # captured on 8 of 24 heads, scaled by 3
+               "vsa_long_video": 14719.0e6}  # captured on 4 of 24 heads, scaled by 6
 
 
 if __name__ == "__main__":

@@ -158,8 +158,10 @@ def _sampled_full_size(w, samples):
     torch.cuda.synchronize()
     code, detail = binding.vsa_device_status()
     assert code == binding.VSA_OK, hex(detail)
-    dq, dk, dv = (t.float().cpu().numpy().astype(np.float64) for t in (dq, dk, dv))
+    # bf16 on the host; only the sampled slices are widened below
+    dq, dk, dv = (t.cpu() for t in (dq, dk, dv))
     del q, k, v, idx, num, vbs, out, lse
+    wide = lambda t: t.float().numpy().astype(np.float64)
 
     blk, nb, D = w.block, w.nb, w.D
     mask = orc.lut_to_blockmask(w.q2k_idx, w.q2k_num, nb)  # [B, H, nb, nb]
@@ -187,12 +189,12 @@ def _sampled_full_size(w, samples):
     ref = {"dq": [], "dk": [], "dv": []}
     for s, ((b, h, kb), col) in enumerate(zip(samples, cols)):
         keys = slice(kb * blk, (kb + 1) * blk)
-        got["dk"].append(dk[b, h, keys])
+        got["dk"].append(wide(dk[b, h, keys]))
         ref["dk"].append(rk[0, s, keys])
-        got["dv"].append(dv[b, h, keys])
+        got["dv"].append(wide(dv[b, h, keys]))
         ref["dv"].append(rv[0, s, keys])
         for t, qb in enumerate(col):
-            got["dq"].append(dq[b, h, qb * blk:(qb + 1) * blk])
+            got["dq"].append(wide(dq[b, h, qb * blk:(qb + 1) * blk]))
             ref["dq"].append(rq[0, s, t * blk:(t + 1) * blk])
     for name in ("dq", "dk", "dv"):
         g, r = np.concatenate(got[name]), np.concatenate(ref[name])
@@ -213,3 +215,11 @@ def test_blk128_workload_sampled_full_size():
     # last key blocks, both batches, several heads
     w = workloads.make("vsa_blk128")
     _sampled_full_size(w, [(0, 0, 0), (1, 23, 255), (0, 17, 128), (1, 4, 31), (1, 9, 200)])
+
+
+def test_long_video_workload_sampled_full_size():
+    # vsa_long_video (24 heads of 98,304 keys, block 64, 3-D neighbourhood selections):
+    # the first key block, one in the middle of the grid and the last one, whose 32 valid
+    # keys exercise the tail mask, on different heads
+    w = workloads.make("vsa_long_video")
+    _sampled_full_size(w, [(0, 0, 0), (0, 11, 700), (0, 23, 1535)])
