@@ -6,10 +6,11 @@
 // lse), p_ij = 2^(s_ij scale log2 e - lse_i), ds_ij = p_ij (dout_i . v_j - D_i),
 // dq_i = scale sum_j ds_ij k_j, dk_j = scale sum_i ds_ij q_i, dv_j = sum_i p_ij dout_i.
 //
-// Why a second kernel: with 64-key blocks, a CTA of vsa_bwd_kernel.cuh owns a pair of key
-// blocks (M = 128 keys) and walks the union of the query blocks selecting either, so keys
-// of the block a query block did not select are computed and masked (43 % of the MMA work
-// on a 25 %-dense random selection).  Here a CTA owns ONE key block and puts query rows on
+// Why a kernel of its own: the block-128 kernel (vsa_bwd_kernel.cuh) puts the keys of one
+// block on the MMA M dimension (M = 128).  With 64-key blocks that layout needs a pair of
+// key blocks per CTA walking the union of the query blocks selecting either, so keys of
+// the block a query block did not select are computed and masked (43 % of the MMA work on
+// a 25 %-dense random selection).  Here a CTA owns ONE key block and puts query rows on
 // M: a step takes two consecutive entries of the block-map column (two query blocks that
 // both select this key block, 128 rows), so no MMA work is masked except the second half
 // of a chunk's odd last step.  The per-row -lse and -D are then one value per thread.
