@@ -139,14 +139,15 @@ def test_large_gqa_sampled():
 
 
 # --------------------------------------------------- the largest key-block count accepted
+@pytest.mark.parametrize("block", [64, 128])
 @pytest.mark.parametrize("route", ["lut", "mask", "split"])
-def test_max_key_blocks_every_block_selected(route):
-    # 2048 key blocks of 64 keys (VSA_MAX_BLOCKS), every one selected by every query block:
-    # the longest list the kernel builds, a dense row of 131,072 keys
+def test_max_key_blocks_every_block_selected(route, block):
+    # 2048 key blocks (VSA_MAX_BLOCKS), every one selected by every query block: the
+    # longest list the kernel builds, a dense row of 131,072 (block 64) or 262,144 keys
     nbk = binding.MAX_BLOCKS
-    w = workloads.make_random_gqa(1, 2, 1, 128, nbk * 64, 128, 64, nbk, seed=150, n_lo=nbk,
-                                  kind="mask" if route == "mask" else "vsa", vbs_lo=60,
-                                  vbs_hi=64)
+    w = workloads.make_random_gqa(1, 2, 1, 128, nbk * block, 128, block, nbk, seed=150,
+                                  n_lo=nbk, kind="mask" if route == "mask" else "vsa",
+                                  vbs_lo=block - 4, vbs_hi=block)
     assert int(w.q2k_num.min()) == nbk
     out, lse = run_gpu(w, splits=8 if route == "split" else None)
     compare(w, out, lse)
