@@ -462,8 +462,8 @@ def main():
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": TRAFFIC.get(w.name),
                 "peak_source": f"{peak_src} dense bf16 (burst)",
-                "kernel": (("bsa_bwd64_kernel" if w.block == 64 else "bsa_bwd_kernel") +
-                           " (whole vsa_bwd call timed)") if bwd else "bsa_fwd_kernel"}
+                "kernel": f"bsa_bwd_kernel<{w.block}> (whole vsa_bwd call timed)" if bwd
+                          else "bsa_fwd_kernel"}
     if bwd:
         roofline["traffic"] = TRAFFIC_BWD.get(w.name)
 
@@ -510,10 +510,10 @@ def main():
 # same kernel build on the same workload; absent = not measured for the current kernel.
 TRAFFIC = {"vsa_long_video": 2473.4e6,  # captured on 4 of 24 heads, scaled by 6
            "jenga": 385.7e6, "vsa_mid": 183.4e6, "vsa_blk128": 1610.9e6}
-# the same for the backward kernel (bsa_bwd64_kernel for block 64, bsa_bwd_kernel for 128)
-TRAFFIC_BWD = {"vsa_mid": 460.8e6,
-               "vsa_blk128": 3913.3e6,  # captured on 8 of 24 heads, scaled by 3
-               "vsa_long_video": 14719.0e6}  # captured on 4 of 24 heads, scaled by 6
+# the same for the backward kernel (bsa_bwd_kernel<64> or <128>)
+TRAFFIC_BWD = {"vsa_mid": 456.6e6,
+               "vsa_blk128": 3916.4e6,  # captured on 8 of 24 heads, scaled by 3
+               "vsa_long_video": 13593.1e6}  # captured on 4 of 24 heads, scaled by 6
 
 
 if __name__ == "__main__":

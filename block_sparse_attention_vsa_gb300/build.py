@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libvsa_gb300.so")
 SOURCES = [os.path.join(CSRC, "vsa_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("vsa_fwd_kernel.cuh", "vsa_bwd_kernel.cuh", "vsa_bwd64_kernel.cuh",
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("vsa_fwd_kernel.cuh", "vsa_bwd_kernel.cuh",
                                                 "sm103_ptx.cuh")] + [
     os.path.join(ROOT, "include", "vsa.h")]
 

@@ -15,7 +15,6 @@
 
 #include "../../include/vsa.h"
 #include "vsa_fwd_kernel.cuh"
-#include "vsa_bwd64_kernel.cuh"
 #include "vsa_bwd_kernel.cuh"
 
 namespace vsa {
@@ -385,52 +384,31 @@ BwdLayout bwd_layout(long long B, long long Hq, long long Sq, long long Sk, int 
   return l;
 }
 
-// The block-128 backward: one CTA per key block.
-vsa_status launch_bwd128(DeviceInfo* dev, const BwdArgs& a, const void* q, const void* k,
-                         const void* v, const void* dout, long long rows_q, long long kv_heads,
-                         long long n_ctas, cudaStream_t s) {
-  auto kern = bwd::bsa_bwd_kernel;
+// The backward: one CTA per key tile of 128 keys (a key block, or an adjacent pair of
+// block-64 key blocks).
+template <int BLOCK>
+vsa_status launch_bwd(DeviceInfo* dev, const BwdArgs& a, const void* q, const void* k,
+                      const void* v, const void* dout, long long rows_q, long long kv_heads,
+                      long long n_ctas, cudaStream_t s) {
+  auto kern = bwd::bsa_bwd_kernel<BLOCK>;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!dev->bwd_attr_set[1]) {
+    if (!dev->bwd_attr_set[BLOCK == 128]) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)bwd::kSmemBytes) != cudaSuccess)
         return VSA_ERR_CUDA;
-      dev->bwd_attr_set[1] = true;
+      dev->bwd_attr_set[BLOCK == 128] = true;
     }
   }
   if (n_ctas == 0) return VSA_OK;
   // Q and dO: [rows, 128] with 64-row boxes (a step); K and V: [heads, Sk, 128] with
-  // 128-row boxes (a key block)
+  // 128-row boxes (a key tile; the rows of a lone last block-64 key block past the end of
+  // a head read as zeros)
   CUtensorMap tq, tdo, tk, tv;
   if (!make_map(&tq, q, rows_q, 64) || !make_map(&tdo, dout, rows_q, 64) ||
       !make_map_3d(&tk, k, kv_heads, a.Sk) || !make_map_3d(&tv, v, kv_heads, a.Sk))
     return VSA_ERR_CUDA;
   kern<<<(unsigned)n_ctas, bwd::kThreads, bwd::kSmemBytes, s>>>(tq, tdo, tk, tv, a);
-  return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
-}
-
-// The block-64 backward: one CTA per key block, Q/dO in 64-row boxes (one list entry),
-// K/V in 64-row boxes.
-vsa_status launch_bwd64(DeviceInfo* dev, const BwdArgs& a, const void* q, const void* k,
-                        const void* v, const void* dout, long long rows_q, long long kv_heads,
-                        long long n_ctas, cudaStream_t s) {
-  auto kern = bwd64::bsa_bwd64_kernel;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!dev->bwd_attr_set[0]) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)bwd64::kSmemBytes) != cudaSuccess)
-        return VSA_ERR_CUDA;
-      dev->bwd_attr_set[0] = true;
-    }
-  }
-  if (n_ctas == 0) return VSA_OK;
-  CUtensorMap tq, tdo, tk, tv;
-  if (!make_map(&tq, q, rows_q, 64) || !make_map(&tdo, dout, rows_q, 64) ||
-      !make_map_3d(&tk, k, kv_heads, a.Sk, 64) || !make_map_3d(&tv, v, kv_heads, a.Sk, 64))
-    return VSA_ERR_CUDA;
-  kern<<<(unsigned)n_ctas, bwd64::kThreads, bwd64::kSmemBytes, s>>>(tq, tdo, tk, tv, a);
   return cudaGetLastError() == cudaSuccess ? VSA_OK : VSA_ERR_CUDA;
 }
 
@@ -575,9 +553,10 @@ vsa_status vsa_bwd(const vsa_bf16* q, const vsa_bf16* k, const vsa_bf16* v,
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_ns = launch_wait_ns(bwd::kWaitLimitNs);
   a.stall = g_stall.load();
-  const long long n_ctas = (long long)B * Hkv * nbk;  // one CTA per key block
-  st = block == 64 ? launch_bwd64(dev, a, q, k, v, dout, rows, (long long)B * Hkv, n_ctas, s)
-                   : launch_bwd128(dev, a, q, k, v, dout, rows, (long long)B * Hkv, n_ctas, s);
+  a.n_tiles = block == 64 ? (nbk + 1) / 2 : nbk;
+  const long long n_ctas = (long long)B * Hkv * a.n_tiles;
+  st = block == 64 ? launch_bwd<64>(dev, a, q, k, v, dout, rows, (long long)B * Hkv, n_ctas, s)
+                   : launch_bwd<128>(dev, a, q, k, v, dout, rows, (long long)B * Hkv, n_ctas, s);
   if (st != VSA_OK) return st;
   if (n_ctas > 0) ++launches;
   const long long n8 = rows * 16;

@@ -12,13 +12,19 @@
 // Kernels:
 //   bwd_prep_kernel   per query row, one warp each: -D_i, and -lse_i (-inf for a row that
 //                     attends no key, so that every p of the row comes out 0).
-//   bsa_bwd_kernel    block 128 (block 64 has its own kernel, vsa_bwd64_kernel.cuh): one CTA
-//                     per (batch, key/value head, key block of 128 keys).  K and V of the
-//                     block stay in SMEM and dK, dV accumulate in TMEM while the CTA walks
-//                     the (query head of the group, query block) pairs selecting the block
-//                     -- a column of the 0/1 block map, compacted into an SMEM list -- 64
-//                     query rows a step (two steps per query block).  Per step, on the
-//                     5th-generation tensor cores:
+//   bsa_bwd_kernel    one CTA per (batch, key/value head, key tile of 128 keys): a tile is
+//                     one key block (block 128) or an adjacent pair of key blocks (block
+//                     64).  K and V of the tile stay in SMEM and dK, dV accumulate in TMEM
+//                     while the CTA walks the (query head of the group, query block) pairs
+//                     selecting the tile -- a column of the 0/1 block map, compacted into
+//                     an SMEM list -- 64 query rows a step (two steps per block-128 query
+//                     block, one per block-64 query block).  A block-64 pair walks the
+//                     union of the query blocks selecting either of its key blocks; each
+//                     list entry says which of the two it selects, and the keys of the
+//                     other are masked.  With neighbourhood selections, where adjacent key
+//                     blocks are selected by mostly the same query blocks, the pair loads
+//                     each shared query block's Q/dO and reduces its dQ once instead of
+//                     twice.  Per step, on the 5th-generation tensor cores:
 //                       S^T  = K Q^T      (M = 128 keys, N = 64 queries, K = d) -> TMEM
 //                       dP^T = V dO^T                                           -> TMEM
 //                       P^T, dS^T formed by the gradient warps (one thread per key row);
@@ -122,6 +128,7 @@ struct BwdArgs {
   uint16_t *dk, *dv;        // [B*Hkv*Sk, 128] bf16
   unsigned int* status;     // device status word
   int Hq, Hkv, group, Sq, Sk, nbq, nbk;
+  int n_tiles;              // key tiles of 128 keys per key/value head
   float scale, scale_log2;
   unsigned long long wait_ns;  // limit of the waits that are not drains (kWaitLimitNs)
   int stall;                // test hook: the MMA warp first waits on a barrier nobody completes
@@ -210,19 +217,22 @@ __device__ __forceinline__ void red_add_f32(float* addr, float x) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(x) : "memory");
 }
 
-// list entry: bits 0-15 query block, bits 20-31 query head within the group.  First
-// query row of step `sub` (64 rows a step) of a block of `block` rows.
+// list entry: bits 0-15 query block, bits 16-17 which key block(s) of the tile it selects
+// (block 64: bit i = key rows 64 i .. 64 i + 63; block 128: bit 0), bits 20-31 query head
+// within the group.  First query row of step `sub` (64 rows a step) of a block of `block`
+// rows.
 __device__ __forceinline__ long long entry_row0(uint32_t e, int sub, const BwdArgs& a, int b,
                                                 int hk, int block) {
   const long long bh = (long long)b * a.Hq + hk * a.group + (int)(e >> 20);
   return bh * a.Sq + (long long)(e & 0xFFFFu) * block + sub * 64;
 }
 
+template <int BLOCK>
 __global__ void __launch_bounds__(kThreads, 1)
     bsa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                    const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                    const BwdArgs a) {
-  constexpr int kSubQ = 2;  // 64-row steps per 128-row query block
+  constexpr int kSubQ = BLOCK / 64;  // 64-row steps per query block
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -231,13 +241,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = (int)(threadIdx.x >> 5);
   const uint32_t lane = threadIdx.x & 31;
 
-  const int tile = (int)(blockIdx.x % (unsigned)a.nbk);   // the CTA's key block
-  const int bkv = (int)(blockIdx.x / (unsigned)a.nbk);    // b * Hkv + hk
+  const int tile = (int)(blockIdx.x % (unsigned)a.n_tiles);   // the CTA's key tile
+  const int bkv = (int)(blockIdx.x / (unsigned)a.n_tiles);    // b * Hkv + hk
   const int b = bkv / a.Hkv, hk = bkv - b * a.Hkv;
-  int vk = 128;  // valid keys of the block
-  if (a.vbs != nullptr) {
-    const int v = a.vbs[tile];
-    vk = v < 0 ? 0 : (v > 128 ? 128 : v);
+  // valid keys of the tile's key block(s): vk[i] for key rows 64 i .. (block 64)
+  int vk[2] = {0, 0};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int kb = BLOCK == 64 ? 2 * tile + i : tile;
+    if ((BLOCK == 64 || i == 0) && kb < a.nbk) {
+      const int v = a.vbs != nullptr ? a.vbs[kb] : BLOCK;
+      vk[i] = v < 0 ? 0 : (v > BLOCK ? BLOCK : v);
+    }
   }
 
   if (threadIdx.x == 0) {
@@ -291,18 +306,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       int cnt = 0;
       while (scan_h < a.group && cnt + 128 <= kMaxEntries) {
         const long long bh = (long long)b * a.Hq + hk * a.group + scan_h;
-        bool sel[4];
+        uint32_t sel[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int qb = scan_qb + 32 * u + (int)lane;
-          sel[u] = qb < a.nbq && a.bitmap[(bh * a.nbq + qb) * (long long)a.nbk + tile] != 0;
+          sel[u] = 0;
+          if (qb < a.nbq) {
+            const int8_t* row = a.bitmap + (bh * a.nbq + qb) * (long long)a.nbk;
+            if (BLOCK == 128) {
+              sel[u] = row[tile] != 0 ? 1u : 0u;
+            } else {
+              sel[u] = row[2 * tile] != 0 ? 1u : 0u;
+              if (2 * tile + 1 < a.nbk && row[2 * tile + 1] != 0) sel[u] |= 2u;
+            }
+          }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint32_t ballot = __ballot_sync(0xffffffffu, sel[u]);
+          const uint32_t ballot = __ballot_sync(0xffffffffu, sel[u] != 0);
           if (sel[u])
             list[cnt + __popc(ballot & ((1u << lane) - 1u))] =
-                ((uint32_t)scan_h << 20) | (uint32_t)(scan_qb + 32 * u + lane);
+                ((uint32_t)scan_h << 20) | (sel[u] << 16) | (uint32_t)(scan_qb + 32 * u + lane);
           cnt += __popc(ballot);
         }
         scan_qb += 128;
@@ -344,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const long long row0 = entry_row0(list[i / kSubQ], i % kSubQ, a, b, hk, 128);
+          const long long row0 = entry_row0(list[i / kSubQ], i % kSubQ, a, b, hk, BLOCK);
           uint8_t* qs = smem + kOffQ + st * kQTile;
           uint8_t* os = smem + kOffDO + st * kQTile;
           float* rs = reinterpret_cast<float*>(smem + kOffRow + st * 512);
@@ -484,10 +508,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp < 8) {
       // ---------------------------------------------------------------- P^T and dS^T
       const int wg = warp >> 2;
-      const int r = (warp & 3) * 32 + (int)lane;  // key row of the block
-      const bool valid = r < vk;
+      const int r = (warp & 3) * 32 + (int)lane;  // key row of the tile
+      const int kbi = BLOCK == 64 ? (r >> 6) : 0;
+      const bool key_ok = (r & (BLOCK - 1)) < (kbi ? vk[1] : vk[0]);
       for (int i = 0; i < n_steps; ++i) {
         const uint32_t gg = g0 + i, st = gg % kStages, b = gg & 1;
+        // block 64: this half of the tile is key block kbi, which the entry may not select
+        const bool valid = BLOCK == 128 ? key_ok
+                                        : key_ok && ((list[i / kSubQ] >> (16 + kbi)) & 1u);
         const uint32_t tS = tmem + lane_base + kColSlot * b + 32 * wg, tDP = tS + kColDPOff;
         uint8_t* ds_row = smem + kOffDS + b * kDSTile + (r >> 3) * 1024 + (r & 7) * 128;
         const float* nlse_s = reinterpret_cast<const float*>(smem + kOffRow + st * 512) + 32 * wg;
@@ -590,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int d = (warp & 3) * 32 + (int)lane;  // d column (TMEM lane of dQ^T)
       for (int i = 0; i < n_steps; ++i) {
         const uint32_t gg = g0 + i, db = gg & 1;
-        const long long row0 = entry_row0(list[i / kSubQ], i % kSubQ, a, b, hk, 128);
+        const long long row0 = entry_row0(list[i / kSubQ], i % kSubQ, a, b, hk, BLOCK);
         if (!wait_warp(&ctl->dq_full[db], (gg >> 1) & 1, ctl, a, 0x4b)) {
           ok = false;
           break;
@@ -637,6 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 8) {
     const int r = (warp & 3) * 32 + (int)lane;
     const bool is_dk = warp >= 4;
+    const bool row_ok = BLOCK == 128 || 128 * tile + r < a.Sk;  // a lone last block-64 key block
     const float sc = is_dk ? a.scale : 1.0f;
     uint16_t* dst = (is_dk ? a.dk : a.dv) + ((long long)bkv * a.Sk + 128 * tile + r) * 128;
     bool have = false;
@@ -655,13 +684,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = 0u;  // no query row attends this block
         }
+        if (row_ok) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          reinterpret_cast<uint4*>(dst + 32 * c)[j] = make_uint4(
-              pack_bf16x2(__uint_as_float(v[8 * j]) * sc, __uint_as_float(v[8 * j + 1]) * sc),
-              pack_bf16x2(__uint_as_float(v[8 * j + 2]) * sc, __uint_as_float(v[8 * j + 3]) * sc),
-              pack_bf16x2(__uint_as_float(v[8 * j + 4]) * sc, __uint_as_float(v[8 * j + 5]) * sc),
-              pack_bf16x2(__uint_as_float(v[8 * j + 6]) * sc, __uint_as_float(v[8 * j + 7]) * sc));
+          for (int j = 0; j < 4; ++j)
+            reinterpret_cast<uint4*>(dst + 32 * c)[j] = make_uint4(
+                pack_bf16x2(__uint_as_float(v[8 * j]) * sc, __uint_as_float(v[8 * j + 1]) * sc),
+                pack_bf16x2(__uint_as_float(v[8 * j + 2]) * sc, __uint_as_float(v[8 * j + 3]) * sc),
+                pack_bf16x2(__uint_as_float(v[8 * j + 4]) * sc, __uint_as_float(v[8 * j + 5]) * sc),
+                pack_bf16x2(__uint_as_float(v[8 * j + 6]) * sc, __uint_as_float(v[8 * j + 7]) * sc));
+        }
       }
     }
   }

@@ -315,8 +315,8 @@ VSA_API int vsa_last_launch_count(void);
  *     0 restores the full limit.  A short limit makes waits run out on ordinary work.
  *   vsa_set_stall_test(enable): while nonzero, the MMA warp of every CTA first waits on
  *     a barrier that nothing ever completes; that wait runs out after the limit above,
- *     records its code in the device status word (forward 0x11f, backward 0x15f for
- *     block 128 and 0x16f for block 64), and every role of the CTA returns.  The launch's outputs are then undefined and
+ *     records its code in the device status word (forward 0x11f, backward 0x15f), and
+ *     every role of the CTA returns.  The launch's outputs are then undefined and
  *     vsa_device_status() reports VSA_ERR_DEVICE_TIMEOUT. */
 VSA_API void vsa_set_wait_limit_ns(unsigned long long ns);
 VSA_API void vsa_set_stall_test(int enable);

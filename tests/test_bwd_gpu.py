@@ -119,9 +119,10 @@ def test_backward_column_longer_than_one_list_chunk():
 @pytest.mark.parametrize("block", [64, 128])
 def test_backward_odd_column_lengths(block):
     """Key blocks selected by 1, 3, 0 and 5 query blocks (of 6, two query heads sharing a
-    key/value head, so 2, 6, 0, 10 entries; and 1, 3, 0, 5 with one head): with block 64 a
-    step takes two entries, so an odd column ends in a step whose second half is padding;
-    a key block nobody selects gets dk = dv = 0."""
+    key/value head, so 2, 6, 0, 10 entries; and 1, 3, 0, 5 with one head).  With block 64
+    the key tile pairs blocks 0 and 1 (whose query blocks partly differ, so entries select
+    one or both) and blocks 2 and 3, where block 2, which nobody selects, shares the tile
+    with block 3; a key block nobody selects gets dk = dv = 0."""
     for hq in (1, 2):
         w = workloads.make_random_gqa(1, hq, 1, 6 * block, 4 * block, 128, block, 4,
                                       seed=140 + hq, vbs_lo=block // 2, vbs_hi=block)

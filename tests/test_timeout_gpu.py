@@ -122,7 +122,8 @@ def test_forward_short_limit_gives_up_mid_pipeline(hooks):
 
 @pytest.mark.parametrize("block", [64, 128])
 def test_backward_stall_reports_timeout(hooks, block):
-    """Both backward kernels (one per block size) unwind from a stalled MMA warp."""
+    """The backward kernel unwinds from a stalled MMA warp, on 128-key blocks and on
+    pairs of 64-key blocks."""
     from block_sparse_attention_vsa_gb300 import workloads
     binding = hooks
     w = workloads.make_random_vsa(1, 2, 8 * block, 128, block, 4, seed=47, n_lo=1)
