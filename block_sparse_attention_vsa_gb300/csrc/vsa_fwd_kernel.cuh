@@ -41,7 +41,8 @@
 //               one 64-column half of the output; warpgroup 0 writes lse.  The store
 //               leader releases that Q buffer only after the next item's first tile,
 //               so the store's read of SMEM never holds up an item boundary.
-//   warp 11     idle.
+//   warp 11     at the start, copies variable_block_sizes (clamped) into SMEM for the list
+//               warp's compaction; then idle.
 // TMEM (512 columns): S0, S1 at columns 0, 128 (warpgroup w reads S columns 64w..64w+63
 // and writes its bf16 P over the first 32 of them); O0, O1 at 256, 384.
 // Every mbarrier wait is bounded; a wait that runs out records a code in the device
@@ -79,9 +80,12 @@ constexpr uint32_t kOffList = kOffKV + kStages * kTileBytes;  // list[2][kMaxNb]
 constexpr uint32_t kOffBm = kOffList + 2 * kMaxNb * 4;       // byte maps [2][kMaxNb]
 constexpr uint32_t kOffStats = kOffBm + 2 * kMaxNb;          // [item parity][wg][3][128] f32
 constexpr uint32_t kStatsBytes = 2 * 2 * 3 * 128 * 4;
-constexpr uint32_t kOffCtl = kOffStats + kStatsBytes;
+constexpr uint32_t kOffVbs = kOffStats + kStatsBytes;  // valid keys per key block [kMaxNb] u8
+constexpr uint32_t kOffCtl = kOffVbs + kMaxNb;
 constexpr uint32_t kCtlBytes = 1024;
 constexpr uint32_t kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "forward SMEM");
+static_assert(kOffCtl % 8 == 0, "control block alignment");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S0, S1
@@ -110,6 +114,7 @@ struct SmemCtl {
   uint64_t stats_bar[2];
   uint64_t epi_bar[2];
   uint64_t drain;
+  uint64_t vbs_ready;  // warp 11 has copied variable_block_sizes into SMEM
   uint64_t never;   // completed by nobody (the timeout test hook waits on it)
   int hdr_item[2];  // work unit (item * n_splits + split), -1 = no more work
   int hdr_n[2];     // list entries of the unit
@@ -231,17 +236,48 @@ __device__ ItemHead build_list(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, ui
     const bool pair = C::kPairs == 2 && h.qa + 1 < a.nbq;  // the second query block exists
     // the item's selection as byte maps (which start, and are always left, all zero)
     if (!JENGA) {
+      // The rows' counts and their first 128 slots are loaded together, before any store
+      // to the byte maps (a store there may not be moved above a later load, so loads
+      // interleaved with stores would each wait a round trip).  Slots past a row's count
+      // lie inside the caller's LUT row and are read but never used.
+      const long long row0 = (long long)h.bh * a.nbq + h.qa;
+      const int rows = (C::kPairs == 2 && pair) ? 2 : 1;
+      const int32_t* lut0 = a.q2k_idx + row0 * a.max_kv;
+      const int32_t* lut1 = lut0 + a.max_kv;
+      const int cnt = (int)lane < rows ? __ldg(a.q2k_num + row0 + lane) : 0;
+      int kb0[4], kb1[4];
 #pragma unroll
-      for (int hf = 0; hf < C::kPairs; ++hf) {
-        if (hf == 1 && !pair) break;
-        const long long row = (long long)h.bh * a.nbq + h.qa + hf;
-        int n = a.q2k_num[row];
-        n = n < 0 ? 0 : (n > a.max_kv ? a.max_kv : n);
-        const int32_t* lut = a.q2k_idx + row * a.max_kv;
+      for (int j = 0; j < 4; ++j) {
+        const int s = 32 * j + (int)lane;
+        kb0[j] = s < a.max_kv ? __ldg(lut0 + s) : -1;
+        kb1[j] = (rows == 2 && s < a.max_kv) ? __ldg(lut1 + s) : -1;
+      }
+      int n0 = __shfl_sync(0xffffffffu, cnt, 0);
+      int n1 = __shfl_sync(0xffffffffu, cnt, 1);
+      n0 = n0 < 0 ? 0 : (n0 > a.max_kv ? a.max_kv : n0);
+      n1 = rows == 2 ? (n1 < 0 ? 0 : (n1 > a.max_kv ? a.max_kv : n1)) : 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int s = 32 * j + (int)lane;
+        if (s < n0 && kb0[j] >= 0 && kb0[j] < nb) bm0[kb0[j]] = 1;
+        if (s < n1 && kb1[j] >= 0 && kb1[j] < nb) bm1[kb1[j]] = 1;
+      }
+      // slots 128 and on (a LUT wider than 128), four loads per lane at a time
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int n = hf ? n1 : n0;
+        const int32_t* lut = hf ? lut1 : lut0;
         uint8_t* bm = hf ? bm1 : bm0;
-        for (int s = lane; s < n; s += 32) {
-          const int kb = lut[s];
-          if (kb >= 0 && kb < nb) bm[kb] = 1;
+        for (int s0 = 128; s0 < n; s0 += 128) {
+          int kbv[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int s = s0 + 32 * j + (int)lane;
+            kbv[j] = s < n ? __ldg(lut + s) : -1;
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (kbv[j] >= 0 && kbv[j] < nb) bm[kbv[j]] = 1;
         }
       }
     } else {
@@ -270,14 +306,15 @@ __device__ ItemHead build_list(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, ui
       if (kb >= nb) return 0u;
       return (uint32_t)bm0[kb] | (C::kPairs == 2 ? (uint32_t)bm1[kb] << 1 : 0u);
     };
+    // (the CTA's copy of variable_block_sizes, already clamped to [0, BLOCK])
     auto valid_keys = [&](int kb) -> int {
-      int valid = BLOCK;
-      if (a.vbs != nullptr) {
-        valid = a.vbs[kb];
-        valid = valid < 0 ? 0 : (valid > BLOCK ? BLOCK : valid);
-      }
-      return valid;
+      return a.vbs != nullptr ? (int)smem[kOffVbs + kb] : BLOCK;
     };
+    // the block sizes the compaction reads come from warp 11's copy
+    if (it == 0 && a.vbs != nullptr && !wait_warp(&ctl->vbs_ready, 0, ctl, a, 9)) {
+      ok = false;
+      return h;
+    }
     const uint32_t below = (1u << lane) - 1u;
     if (C::kPairs == 1) {
       // ascending compaction
@@ -861,6 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->o_full, 1);
     mbar_init(&ctl->o_empty, 8);
     mbar_init(&ctl->drain, 1);
+    mbar_init(&ctl->vbs_ready, 1);
     mbar_init(&ctl->never, 1);
     ctl->abort_flag = 0;
     fence_mbar_init();
@@ -898,6 +936,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 9) {
       if (lane_id() == 0) mma_role<BLOCK, JENGA>(smem, ctl, a, tmem);
       __syncwarp();
+    } else if (warp == 11 && a.vbs != nullptr) {
+      // variable_block_sizes, clamped, into SMEM once per CTA, while the list warp loads
+      // the first item's LUT rows: the compaction reads one entry per selected block, and
+      // from global memory each would cost a round trip of its own
+      const uint32_t lane = lane_id();
+      uint8_t* vt = smem + kOffVbs;
+      for (int base = 0; base < a.nbk; base += 32 * 16) {
+        int v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int kb = base + 32 * j + (int)lane;
+          v[j] = kb < a.nbk ? __ldg(a.vbs + kb) : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int kb = base + 32 * j + (int)lane;
+          if (kb < a.nbk) vt[kb] = (uint8_t)(v[j] < 0 ? 0 : (v[j] > BLOCK ? BLOCK : v[j]));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->vbs_ready);
     }
   }
 
