@@ -321,11 +321,9 @@ __device__ ItemHead build_list(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, ui
       for (int base = 0; base < nb; base += 32) {
         const int kb = base + (int)lane;
         const uint32_t sel = selected(kb);
+        const int valid = kb < nb ? valid_keys(kb) : 0;
         const uint32_t ballot = __ballot_sync(0xffffffffu, sel != 0);
-        if (sel) {
-          list[count + __popc(ballot & below)] = make_entry(kb, 3u, valid_keys(kb));
-          bm0[kb] = 0;
-        }
+        if (sel) list[count + __popc(ballot & below)] = make_entry(kb, 3u, valid);
         count += __popc(ballot);
       }
     } else {
@@ -348,29 +346,31 @@ __device__ ItemHead build_list(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, ui
       for (int base = 0; base < nb; base += 32) {
         const int kb = base + (int)lane;
         const uint32_t sel = selected(kb);
+        const int valid = kb < nb ? valid_keys(kb) : 0;
         const uint32_t bx = __ballot_sync(0xffffffffu, sel == 1u);
         const uint32_t by = __ballot_sync(0xffffffffu, sel == 2u);
         const uint32_t bb = __ballot_sync(0xffffffffu, sel == 3u);
-        if (sel) {
-          int pos;
-          if (sel == 1u) {
-            const int i = cx + __popc(bx & below);
-            pos = i < xy ? 2 * i : 2 * xy + (i - xy);
-          } else if (sel == 2u) {
-            const int i = cy + __popc(by & below);
-            pos = i < xy ? 2 * i + 1 : 2 * xy + (i - xy);
-          } else {
-            pos = 2 * xy + rest + cb + __popc(bb & below);
-          }
-          list[pos] = make_entry(kb, sel, valid_keys(kb));
-          bm0[kb] = 0;
-          bm1[kb] = 0;
-        }
+        // this block's rank among the blocks of its kind so far (selects, no branches)
+        const uint32_t mine = sel == 1u ? bx : (sel == 2u ? by : bb);
+        const int i = (sel == 1u ? cx : (sel == 2u ? cy : cb)) + __popc(mine & below);
+        const int single = i < xy ? 2 * i + (sel == 2u ? 1 : 0) : 2 * xy + (i - xy);
+        const int pos = sel == 3u ? 2 * xy + rest + i : single;
+        if (sel) list[pos] = make_entry(kb, sel, valid);
         cx += __popc(bx);
         cy += __popc(by);
         cb += __popc(bb);
       }
       count = nx + ny + cb;
+    }
+    __syncwarp();
+    // leave the byte maps all zero for the next item (16-byte stores; the compaction
+    // loops above only read them)
+    {
+      uint4* z = reinterpret_cast<uint4*>(bm0);
+      const int words = (C::kPairs == 2 ? 2 * kMaxNb : kMaxNb) / 16;
+      const int used = (nb + 15) / 16;  // words of each map that can hold a 1
+      for (int i = (int)lane; i < words; i += 32)
+        if ((i % (kMaxNb / 16)) < used) z[i] = make_uint4(0u, 0u, 0u, 0u);
     }
     __syncwarp();
     if (a.n_splits > 1) {
