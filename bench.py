@@ -508,8 +508,8 @@ def main():
 
 # DRAM bytes (read + write) per launch of the forward kernel, from an ncu capture of the
 # same kernel build on the same workload; absent = not measured for the current kernel.
-TRAFFIC = {"vsa_long_video": 2438.9e6,  # captured on 4 of 24 heads, scaled by 6
-           "jenga": 384.4e6, "vsa_mid": 183.0e6, "vsa_blk128": 1610.5e6}
+TRAFFIC = {"vsa_long_video": 2454.0e6,  # captured on 4 of 24 heads, scaled by 6
+           "jenga": 384.6e6, "vsa_mid": 182.7e6, "vsa_blk128": 1610.7e6}
 # the same for the backward kernel (bsa_bwd_kernel<64> or <128>)
 TRAFFIC_BWD = {"vsa_mid": 456.6e6,
                "vsa_blk128": 3916.4e6,  # captured on 8 of 24 heads, scaled by 3

@@ -310,12 +310,16 @@ __device__ ItemHead build_list(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, ui
     auto valid_keys = [&](int kb) -> int {
       return a.vbs != nullptr ? (int)smem[kOffVbs + kb] : BLOCK;
     };
-    // the block sizes the compaction reads come from warp 11's copy
-    if (it == 0 && a.vbs != nullptr && !wait_warp(&ctl->vbs_ready, 0, ctl, a, 9)) {
+    // the block sizes the compaction reads come from warp 11's copy (block-64 pairs wait
+    // after their counting pass, which does not read them)
+    auto sizes_ready = [&]() -> bool {
+      return it != 0 || a.vbs == nullptr || wait_warp(&ctl->vbs_ready, 0, ctl, a, 9);
+    };
+    const uint32_t below = (1u << lane) - 1u;
+    if (C::kPairs == 1 && !sizes_ready()) {
       ok = false;
       return h;
     }
-    const uint32_t below = (1u << lane) - 1u;
     if (C::kPairs == 1) {
       // ascending compaction
       for (int base = 0; base < nb; base += 32) {
@@ -339,6 +343,10 @@ __device__ ItemHead build_list(uint8_t* smem, SmemCtl* ctl, const FwdArgs& a, ui
         const uint32_t sel = selected(base + (int)lane);
         nx += __popc(__ballot_sync(0xffffffffu, sel == 1u));
         ny += __popc(__ballot_sync(0xffffffffu, sel == 2u));
+      }
+      if (!sizes_ready()) {
+        ok = false;
+        return h;
       }
       const int xy = nx < ny ? nx : ny;
       const int rest = (nx - xy) + (ny - xy);
