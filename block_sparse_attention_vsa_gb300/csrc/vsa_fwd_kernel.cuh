@@ -1003,25 +1003,61 @@ __global__ void __launch_bounds__(256) split_merge_kernel(const float* __restric
   if (qrow >= Sq) return;  // the rows past a lone last query block
   const uint32_t lane = threadIdx.x & 31;
   const float* p0 = part + (size_t)item * n_splits * kPartFloats;
-  float M = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) {
-    const float* st = p0 + (size_t)s * kPartFloats + 128 * 128;
-    if (st[128 + row] > 0.0f) M = fmaxf(M, st[row]);
+  // the row's statistics of splits lane and lane + 32 (n_splits <= 64), read in parallel
+  float m[2], l_r[2], l_e[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = (int)lane + 32 * h;
+    m[h] = -INFINITY;
+    l_r[h] = 0.0f;
+    l_e[h] = 0.0f;
+    if (s < n_splits) {
+      const float* st = p0 + (size_t)s * kPartFloats + 128 * 128;
+      m[h] = st[row];
+      l_r[h] = st[128 + row];
+      l_e[h] = st[256 + row];
+    }
   }
-  float lr = 0.0f, le = 0.0f;
+  float M = -INFINITY;
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    if (l_r[h] > 0.0f) M = fmaxf(M, m[h]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float c[2], lr = 0.0f, le = 0.0f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    c[h] = l_r[h] > 0.0f ? exp2f(m[h] - M) : 0.0f;
+    lr = fmaf(c[h], l_r[h], lr);
+    le = fmaf(c[h], l_e[h], le);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lr += __shfl_xor_sync(0xffffffffu, lr, o);
+    le += __shfl_xor_sync(0xffffffffu, le, o);
+  }
+  // O: this lane's 4 columns of each split's partial, four splits' loads at a time, summed
+  // in split order
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < n_splits; ++s) {
-    const float* ps = p0 + (size_t)s * kPartFloats;
-    const float l_r = ps[128 * 128 + 128 + row];
-    if (!(l_r > 0.0f)) continue;
-    const float c = exp2f(ps[128 * 128 + row] - M);
-    lr = fmaf(c, l_r, lr);
-    le = fmaf(c, ps[128 * 128 + 256 + row], le);
-    const float4 o = reinterpret_cast<const float4*>(ps + row * 128)[lane];
-    acc.x = fmaf(c, o.x, acc.x);
-    acc.y = fmaf(c, o.y, acc.y);
-    acc.z = fmaf(c, o.z, acc.z);
-    acc.w = fmaf(c, o.w, acc.w);
+  for (int s0 = 0; s0 < n_splits; s0 += 4) {
+    float cs[4];
+    float4 o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int s = s0 + j;
+      const float cj = __shfl_sync(0xffffffffu, (s & 32) ? c[1] : c[0], s & 31);
+      cs[j] = s < n_splits ? cj : 0.0f;
+      o[j] = cs[j] != 0.0f
+                 ? reinterpret_cast<const float4*>(p0 + (size_t)s * kPartFloats + row * 128)[lane]
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc.x = fmaf(cs[j], o[j].x, acc.x);
+      acc.y = fmaf(cs[j], o[j].y, acc.y);
+      acc.z = fmaf(cs[j], o[j].z, acc.z);
+      acc.w = fmaf(cs[j], o[j].w, acc.w);
+    }
   }
   const bool has = lr > 0.0f;
   const float inv = has ? 1.0f / lr : 0.0f;
