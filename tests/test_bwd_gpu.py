@@ -140,6 +140,30 @@ def test_backward_odd_column_lengths(block):
         assert not dk[0, 0, rows].float().abs().any() and not dv[0, 0, rows].float().abs().any()
 
 
+
+def test_backward_block64_pairs_one_sided_and_lone_last_block():
+    """Block 64 runs key blocks in adjacent pairs.  Five key blocks (the last pair is a lone
+    block whose partner rows lie past the end of the keys): pair (0, 1) has query blocks
+    selecting only block 0, only block 1 and both; in pair (2, 3) only block 3 is selected;
+    the lone block 4 is selected with a 40-key tail.  Two query heads share a key/value
+    head, so a column mixes heads."""
+    w = workloads.make_random_gqa(1, 2, 1, 6 * 64, 5 * 64, 128, 64, 4, seed=151,
+                                  vbs_lo=64, vbs_hi=64)
+    w.vbs[4] = 40
+    sel = {0: [0, 2], 1: [1, 2, 5], 2: [], 3: [0, 4], 4: [1, 3, 5]}
+    w.q2k_idx[...] = -1
+    w.q2k_num[...] = 0
+    for kb, qbs in sel.items():
+        for qb in qbs:
+            for h in range(2):
+                n = w.q2k_num[0, h, qb]
+                w.q2k_idx[0, h, qb, n] = kb
+                w.q2k_num[0, h, qb] = n + 1
+    dq, dk, dv = run_and_compare(w)
+    rows = slice(2 * 64, 3 * 64)  # key block 2: selected by nobody
+    assert not dk[0, 0, rows].float().abs().any() and not dv[0, 0, rows].float().abs().any()
+    assert not dk[0, 0, 4 * 64 + 40:].float().abs().any()  # the tail keys of block 4
+
 def _sampled_full_size(w, samples):
     """The backward of workload ``w`` at full size, in the launch configuration the
     benchmark times, checked on sampled key blocks ``samples`` = [(b, h, kb)].  The query
